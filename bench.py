@@ -1,0 +1,493 @@
+#!/usr/bin/env python3
+"""Benchmark of the dense GEMM library on one or more GB300 GPUs.
+
+One step is one pass of the whole hot path over one batch of synthetic
+input: the FP32 SGEMM 4096^3 (CUDA cores) followed by the BF16 GEMM 4096^3
+(tcgen05 tensor cores, fp32 accumulate, bf16 out).  `--workload` selects a
+single workload instead (see gemm_inputs/workloads.py).
+
+Timing: W untimed warm-up steps, then K timed steps.  Before every step a
+256 MiB buffer is written to flush the 129 MB L2 (outside the timed events);
+each kernel is bracketed by CUDA events on the stream it is launched on.
+`value` = work of all ranks / the slowest rank's summed step time.  Prints
+one JSON line (rank 0).
+
+`--impl reference` times the CPU oracle instead (the reference arm: the
+plain double-precision triple loop, on the host cores), on a bounded sample
+of rows of the same workload.
+
+Multi-GPU: the GEMM is run as independent replicas, one per rank (no data
+exchange); ranks only meet for a barrier and a max-reduction of times.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (BF16 tcgen05, FP32 SIMT) at 4096^3 and % of chip peak"
+STEP_WORKLOADS = ("sgemm_4096", "bf16_4096")
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+# Published number for the same workload on other hardware (context only):
+# FP32 SGEMM 4096^3, final hand-written version on an RTX 3090.
+PAGE_SGEMM_4096_TFLOPS = 10.23
+FP32_LANES_PER_SM = 128  # FP32 FMA units per Blackwell SM (4 partitions x 32)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workloads_for(name):
+    from gemm_inputs.workloads import WORKLOADS
+
+    if name == "step":
+        return [WORKLOADS[n] for n in STEP_WORKLOADS]
+    if name not in WORKLOADS:
+        raise SystemExit(f"unknown workload {name!r}; choose step or one of {list(WORKLOADS)}")
+    return [WORKLOADS[name]]
+
+
+# ---------------------------------------------------------------- distributed
+
+class Dist:
+    def __init__(self, gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            backend = "nccl" if _cuda_ok() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+        self.gpus = gpus
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        dev = "cuda" if _cuda_ok() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+
+        dev = "cuda" if _cuda_ok() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def _cuda_ok():
+    import torch
+
+    return torch.cuda.is_available()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gemm_bench_clocks_{os.getpid()}.csv")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1])]
+        smax = max((num(r[2]) for r in rows if num(r[2])), default=None)
+        power = [num(r[3]) for r in rows if num(r[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if smax and s > 0.3 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+def _sample_operands(w, rows, B_cache):
+    if w.name not in B_cache:
+        B_cache[w.name] = w.operands(rows=slice(0, 1))[1]
+    A, _, C = w.operands(rows=slice(0, rows))
+    return A, B_cache[w.name], C
+
+
+def oracle_sample_time(workloads, seconds_target):
+    """Times the CPU oracle (all host threads) on the leading rows of each
+    workload, with the row count chosen from a one-row-per-thread
+    calibration so the sample takes about seconds_target.
+    Returns (flops, seconds, rows, threads)."""
+    import oracle
+
+    oracle.build()
+    threads = oracle.default_threads()
+    max_rows = min(w.M for w in workloads)
+    B_cache = {}
+
+    def timed(rows):
+        ops = [(w, *_sample_operands(w, rows, B_cache)) for w in workloads]
+        t0 = time.perf_counter()
+        for w, A, B, C in ops:
+            oracle.gemm(A, B, C, alpha=w.alpha, beta=w.beta, threads=threads)
+        return time.perf_counter() - t0
+
+    cal_rows = min(threads, max_rows)
+    t_cal = timed(cal_rows)
+    rows = int(cal_rows * seconds_target / max(t_cal, 1e-6))
+    rows = max(cal_rows, min(max_rows, (rows // cal_rows) * cal_rows))
+    dt = timed(rows) if rows != cal_rows else t_cal
+    flops = sum(2 * rows * w.N * w.K for w in workloads)
+    return flops, dt, rows, threads
+
+
+def run_reference(args, dist):
+    workloads = workloads_for(args.workload)
+    if dist.rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    threads = oracle.default_threads()
+    # bounded sample: about a minute of oracle work over all steps
+    per_step_target = max(0.2, 60.0 / max(1, args.steps + args.warmup))
+    _flops, _dt, rows, _threads = oracle_sample_time(workloads, per_step_target)
+    B_cache = {}
+    inputs = [(w, *_sample_operands(w, rows, B_cache)) for w in workloads]
+
+    def step():
+        for w, A, B, C in inputs:
+            oracle.gemm(A, B, C, alpha=w.alpha, beta=w.beta, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    flops = args.steps * sum(2 * rows * w.N * w.K for w in workloads)
+    value = flops / dt / 1e12
+    sample = (f"leading {rows} rows of each of {', '.join(w.name for w in workloads)} "
+              f"(full K and N), double-precision triple loop on {threads} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(workloads, args),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def config_block(workloads, args):
+    name = "+".join(w.name for w in workloads)
+    return {
+        "workload": name,
+        "shapes": {w.name: {"M": w.M, "N": w.N, "K": w.K, "in": w.dtype, "out": w.out,
+                            "alpha": w.alpha, "beta": w.beta, "dist": w.description}
+                   for w in workloads},
+        "layout": "row-major A (MxK), B (KxN), C (MxN), contiguous",
+        "l2": "flushed before every step by writing a 256 MiB buffer (outside the timed events)",
+        "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU",
+    }
+
+
+def kernel_source_hash(w):
+    fname = "sgemm_simt.cu" if w.dtype == "f32" else "gemm_bf16_tc.cu"
+    path = os.path.join(ROOT, "dense_gemm_02_gb300", "csrc", fname)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(w):
+    """DRAM bytes per launch from a committed ncu capture of this exact
+    kernel source, else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(w.name)
+    if not rec or rec.get("source_sha256_16") != kernel_source_hash(w):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def run_ours(args, dist):
+    import torch
+
+    import dense_gemm_02_gb300 as g
+    from dense_gemm_02_gb300 import _build
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (use --impl reference for the CPU oracle)")
+    torch.cuda.set_device(dist.local_rank)
+    _build.build()
+    g.binding.lib()
+    workloads = workloads_for(args.workload)
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(dist.local_rank)
+    sms = props.multi_processor_count
+
+    # ---- inputs resident in HBM
+    dev_ops = []
+    host_ops = []
+    for w in workloads:
+        A, B, C = w.operands()
+        if w.dtype == "f32":
+            hA, hB = torch.from_numpy(A), torch.from_numpy(B)
+        else:
+            hA = torch.from_numpy(A.view("int16")).view(torch.bfloat16)
+            hB = torch.from_numpy(B.view("int16")).view(torch.bfloat16)
+        out_dt = torch.float32 if w.out == "f32" else torch.bfloat16
+        if C is not None:
+            hC = (torch.from_numpy(C) if w.out == "f32"
+                  else torch.from_numpy(C.view("int16")).view(torch.bfloat16))
+        else:
+            hC = None
+        dA, dB = hA.cuda(), hB.cuda()
+        dC = hC.cuda() if hC is not None else torch.empty((w.M, w.N), dtype=out_dt,
+                                                            device="cuda")
+        dev_ops.append((w, dA, dB, dC))
+        host_ops.append((w, hA.pin_memory(), hB.pin_memory(),
+                         hC.pin_memory() if hC is not None else None, out_dt))
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def launch(w, dA, dB, dC):
+        if w.dtype == "f32":
+            g.sgemm(dA, dB, dC, alpha=w.alpha, beta=w.beta)
+        else:
+            g.gemm_bf16(dA, dB, dC, alpha=w.alpha, beta=w.beta)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        for op in dev_ops:
+            launch(*op)
+    torch.cuda.synchronize()
+    g.binding.check(g.binding.get_device_status(), "warm-up device status")
+
+    nk = len(dev_ops)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+              for _ in range(args.steps)]
+    clocks = ClockSampler(dist.local_rank)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        ev = events[s]
+        ev[0].record(stream)
+        for i, op in enumerate(dev_ops):
+            launch(*op)
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    clock_info = clocks.stop()
+    g.binding.check(g.binding.get_device_status(), "timed-region device status")
+
+    per_kernel_ms = [[ev[i].elapsed_time(ev[i + 1]) for ev in events] for i in range(nk)]
+    step_ms = [sum(per_kernel_ms[i][s] for i in range(nk)) for s in range(args.steps)]
+    total_s = dist.max(sum(step_ms) / 1e3)
+    flops_step = sum(w.flops for w in workloads)
+    value = dist.sum(flops_step * args.steps) / total_s / 1e12
+    gpu_launches = nk * args.steps
+
+    sm_max = (clock_info or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
+    fp32_peak = sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+
+    kernels = {}
+    rooflines = {}
+    for i, w in enumerate(workloads):
+        ms = statistics.mean(per_kernel_ms[i])
+        tflops = w.flops / (ms / 1e3) / 1e12
+        gbs = w.min_bytes() / (ms / 1e3) / 1e9
+        entry = {"ms_mean": ms, "ms_median": statistics.median(per_kernel_ms[i]),
+                 "ms_min": min(per_kernel_ms[i]), "tflops": tflops, "min_bytes": w.min_bytes(),
+                 "achieved_gbs_min_bytes": gbs}
+        if w.dtype == "f32":
+            rl = {"bound": "alu", "achieved": tflops, "peak": fp32_peak, "unit": "TFLOP/s",
+                  "frac": tflops / fp32_peak, "traffic": recorded_traffic(w),
+                  "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
+                                 f"x {sm_max:.0f} MHz (max SM clock)",
+                  "kernel": "sgemm_simt_kernel"}
+        elif w.M * w.N * w.K / (w.min_bytes() / 2) < 300:  # intensity below the ridge: HBM
+            peak_bw = peaks["hbm_gbs"]
+            rl = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
+                  "frac": gbs / peak_bw, "traffic": recorded_traffic(w),
+                  "peak_source": f"{peak_src} hbm_gbs",
+                  "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
+                  "kernel": "bf16_tc_kernel"}
+        else:
+            pk = peaks["bf16_tflops"]
+            rl = {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s",
+                  "frac": tflops / pk, "traffic": recorded_traffic(w),
+                  "peak_source": f"{peak_src} bf16_tflops (burst)",
+                  "frac_of_sustained": tflops / peaks.get("bf16_tflops_sustained", pk),
+                  "kernel": "bf16_tc_kernel"}
+        kernels[w.name] = entry
+        rooflines[w.name] = rl
+    dominant = max(range(nk), key=lambda i: statistics.mean(per_kernel_ms[i]))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(step_ms), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (value / PAGE_SGEMM_4096_TFLOPS
+                        if [w.name for w in workloads] == ["sgemm_4096"] else None),
+        "dtype": "+".join(sorted({w.dtype for w in workloads})),
+        "data": "synthetic (seeded splitmix64 inputs; shapes and distributions of the workload)",
+        "config": config_block(workloads, args),
+        "roofline": rooflines[workloads[dominant].name],
+        "rooflines": rooflines, "kernels": kernels,
+        "gpu_launches": gpu_launches, "wall_s_timed_region": wall,
+        "clocks": clock_info,
+        "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
+                  "bf16_tflops": peaks["bf16_tflops"], "fp32_tflops_derived": fp32_peak,
+                  "sms": sms},
+    }
+
+    # ---- end to end through the public API with pinned host buffers
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 20))
+        outs = [torch.empty((w.M, w.N), dtype=od, pin_memory=True)
+                for (w, _a, _b, _c, od) in host_ops]
+
+        def e2e_step():
+            for (w, hA, hB, hC, od), out in zip(host_ops, outs):
+                g.gemm(hA, hB, hC, alpha=w.alpha, beta=w.beta, out_dtype=od, out=out)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_s = dist.max(max(e0.elapsed_time(e1) / 1e3, time.perf_counter() - t0))
+        h2d = sum((hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+                   + (hC.numel() * hC.element_size() if (hC is not None and w.beta != 0) else 0))
+                  for (w, hA, hB, hC, od) in host_ops)
+        d2h = sum(o.numel() * o.element_size() for o in outs)
+        line["e2e"] = {"value": dist.sum(flops_step * e2e_steps) / e2e_s / 1e12,
+                       "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                       "api": "dense_gemm_02_gb300.gemm(host pinned tensors)"}
+    else:
+        line["e2e"] = None
+
+    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
+        flops, dt, rows, threads = oracle_sample_time(workloads, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"leading {rows} rows of each of {', '.join(w.name for w in workloads)} "
+                      f"(full K and N), {dt:.1f} s on {threads} threads"}
+    if dist.rank == 0:
+        print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse_args()
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, dist)
+        return run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,131 @@
+"""ctypes binding to libgemm_gb300.so (C ABI in include/gemm_gb300.h).
+
+Argument marshalling only: every arithmetic step runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  If the compiled
+library is missing the import of the entry points raises; there is no CPU
+fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = -1
+GEMM_ERR_NULLPTR = -2
+GEMM_ERR_BAD_LD = -3
+GEMM_ERR_UNSUPPORTED_DEVICE = -4
+GEMM_ERR_CUDA = -5
+GEMM_ERR_DEVICE_TIMEOUT = -6
+GEMM_ERR_ALIAS = -7
+GEMM_ERR_TOO_LARGE = -8
+
+GEMM_OUT_BF16 = 0
+GEMM_OUT_F32 = 1
+
+# Every exported symbol of the C ABI, with (restype, argtypes).
+_i64, _f32, _vp, _int, _cp = (ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
+                              ctypes.c_char_p)
+SIGNATURES = {
+    "gemm_f32": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
+    "gemm_bf16": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _int,
+                         _vp]),
+    "gemm_get_device_status": (_int, [_vp]),
+    "gemm_get_device_fault_info": (_i64, []),
+    "gemm_status_string": (_cp, [_int]),
+    "gemm_set_config": (_int, [_cp, _i64]),
+    "gemm_get_config": (_int, [_cp, ctypes.POINTER(_i64)]),
+    "gemm_last_kernel": (_cp, []),
+    "gemm_shutdown": (_int, []),
+    "gemm_abi_version": (_int, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class GemmError(RuntimeError):
+    """A non-zero gemm_status_t returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib():
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"libgemm_gb300.so is not built ({path}); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        handle = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gemm_status_string(int(status)).decode()
+
+
+def check(status: int, where: str) -> None:
+    if status != GEMM_OK:
+        raise GemmError(status, where)
+
+
+# ------------------------------------------------------------ raw entry points
+
+def gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream) -> int:
+    """Raw call; pointers and stream are integers (device addresses)."""
+    return lib().gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+
+def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream) -> int:
+    """Raw call; A/B/C are device addresses, c_type GEMM_OUT_BF16/F32."""
+    return lib().gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream)
+
+
+def get_device_status(stream=None) -> int:
+    return lib().gemm_get_device_status(stream)
+
+
+def get_device_fault_info() -> int:
+    return int(lib().gemm_get_device_fault_info())
+
+
+def set_config(key: str, value: int) -> None:
+    check(lib().gemm_set_config(key.encode(), int(value)), f"gemm_set_config({key})")
+
+
+def get_config(key: str) -> int:
+    v = ctypes.c_int64(0)
+    check(lib().gemm_get_config(key.encode(), ctypes.byref(v)), f"gemm_get_config({key})")
+    return int(v.value)
+
+
+def last_kernel() -> str:
+    return lib().gemm_last_kernel().decode()
+
+
+def shutdown() -> None:
+    check(lib().gemm_shutdown(), "gemm_shutdown")
+
+
+def abi_version() -> int:
+    return int(lib().gemm_abi_version())

@@ -98,27 +98,31 @@ def splitmix64_stream(seed: int, stream: int, start: int, count: int) -> np.ndar
     return splitmix64_from_state(_stream_state(seed, stream), start, count)
 
 
-def _chunked(n: int, fn) -> np.ndarray:
+def _chunked(n: int, fn, offset: int = 0) -> np.ndarray:
+    """fn(first_index, count) over [offset, offset + n) in chunks."""
     out = np.empty(n, dtype=np.float32)
     for lo in range(0, n, _CHUNK):
         hi = min(n, lo + _CHUNK)
-        out[lo:hi] = fn(lo, hi - lo)
+        out[lo:hi] = fn(offset + lo, hi - lo)
     return out
 
 
-def uniform_f32(seed: int, stream: int, n: int) -> np.ndarray:
-    """n values uniform on the 2**-23 grid of [-1, 1) (exact fp32)."""
+def uniform_f32(seed: int, stream: int, n: int, offset: int = 0) -> np.ndarray:
+    """Elements offset .. offset+n-1: uniform on the 2**-23 grid of [-1, 1)
+    (exact fp32)."""
 
     def gen(lo, cnt):
         x = splitmix64_stream(seed, stream, lo, cnt)
         u = (x >> np.uint64(40)).astype(np.float64)
         return (u * 2.0**-23 - 1.0).astype(np.float32)
 
-    return _chunked(n, gen)
+    return _chunked(n, gen, offset)
 
 
-def normal_f32(seed: int, stream: int, n: int, sigma: float = 1.0) -> np.ndarray:
-    """n values sigma * N(0, 1) by Box-Muller in double, rounded to fp32."""
+def normal_f32(seed: int, stream: int, n: int, sigma: float = 1.0,
+               offset: int = 0) -> np.ndarray:
+    """Elements offset .. offset+n-1: sigma * N(0, 1) by Box-Muller in
+    double, rounded to fp32."""
 
     def gen(lo, cnt):
         x = splitmix64_stream(seed, stream, 2 * lo, 2 * cnt)
@@ -127,17 +131,17 @@ def normal_f32(seed: int, stream: int, n: int, sigma: float = 1.0) -> np.ndarray
         z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
         return (sigma * z).astype(np.float32)
 
-    return _chunked(n, gen)
+    return _chunked(n, gen, offset)
 
 
-def integer_f32(seed: int, stream: int, n: int) -> np.ndarray:
-    """n integers in {-2..2} stored as fp32."""
+def integer_f32(seed: int, stream: int, n: int, offset: int = 0) -> np.ndarray:
+    """Elements offset .. offset+n-1: integers in {-2..2} stored as fp32."""
 
     def gen(lo, cnt):
         x = splitmix64_stream(seed, stream, lo, cnt)
         return ((x % np.uint64(5)).astype(np.int64) - 2).astype(np.float32)
 
-    return _chunked(n, gen)
+    return _chunked(n, gen, offset)
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -163,19 +167,20 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
 
 
 def draw(kind: str, seed: int, stream: int, shape, sigma: float = 1.0,
-         dtype: str = "f32") -> np.ndarray:
-    """One operand of ``shape`` (row-major), drawn from ``kind``.
+         dtype: str = "f32", offset: int = 0) -> np.ndarray:
+    """One operand of ``shape`` (row-major), drawn from ``kind``; its
+    elements are stream elements offset, offset+1, ...
 
     kind: "uniform" | "normal" | "integer"; dtype: "f32" returns float32,
     "bf16" returns the uint16 bf16 bits.
     """
     n = int(np.prod(shape)) if len(shape) else 1
     if kind == "uniform":
-        v = uniform_f32(seed, stream, n)
+        v = uniform_f32(seed, stream, n, offset)
     elif kind == "normal":
-        v = normal_f32(seed, stream, n, sigma)
+        v = normal_f32(seed, stream, n, sigma, offset)
     elif kind == "integer":
-        v = integer_f32(seed, stream, n)
+        v = integer_f32(seed, stream, n, offset)
     else:
         raise ValueError(f"unknown distribution {kind!r}")
     v = v.reshape(shape)

@@ -1,0 +1,164 @@
+/*
+ * gemm_gb300.h -- dense matrix multiply C = alpha * A * B + beta * C on one
+ * NVIDIA GB300 (sm_103a).  C ABI of libgemm_gb300.so.
+ *
+ * The operation is the general GEMM of "Blackwell BF16 GEMM ..." (lshu.cn),
+ * section 1.1 (C = alpha*A*B + beta*C), in the two precisions the pages
+ * treat:
+ *   - gemm_f32:  FP32 SGEMM on the CUDA cores, as in "CUDA hand-written
+ *     SGEMM: 0.4 -> 10.23 TFLOPS" (gtnt.cn), sections 1.1-7.1.  Every
+ *     product and sum is an IEEE fp32 fused multiply-add; nothing is rounded
+ *     through TF32.
+ *   - gemm_bf16: BF16 operands, FP32 accumulation in the tensor cores, one
+ *     final conversion to BF16 (or an FP32 store), as in "Blackwell BF16
+ *     GEMM ...", sections 1.2, 2.1-2.3 and 6.3.
+ *
+ * Layout.  All matrices are row-major.  A is M x K with row pitch lda >= K,
+ * B is K x N with row pitch ldb >= N, C is M x N with row pitch ldc >= N.
+ * Pitches count elements, not bytes.
+ *
+ * Memory and ownership.  A, B and C are DEVICE pointers owned by the caller
+ * (for example torch tensors); the library never frees or retains them.
+ * Pointers need only element alignment.  The fast paths (TMA, 16-byte
+ * vectors) are taken when base addresses are 16-byte aligned and
+ * pitch * element size is a multiple of 16 bytes; otherwise a slower
+ * generic GPU kernel runs.  There is no CPU fallback.
+ *
+ * Semantics (the BLAS conventions):
+ *   - M == 0 or N == 0: nothing is done.
+ *   - beta == 0: C is not read (it may hold NaN or garbage).
+ *   - alpha == 0 or K == 0: A and B are not read; C = beta * C.
+ *   - C must not overlap A or B (checked by address range).
+ *   - BF16 outputs are rounded to nearest, ties to even; overflow gives inf.
+ *   - For a given call configuration results are bit-for-bit reproducible
+ *     from run to run (no floating-point atomics).
+ *
+ * Streams and errors.  Calls enqueue work on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and return without synchronising.  The
+ * return value is a gemm_status_t: argument errors are found on the host
+ * before anything is launched; GEMM_ERR_CUDA means a CUDA call failed at
+ * launch.  Device-side faults of the pipeline (a wait that ran past its
+ * time limit) are recorded in a per-device status word that
+ * gemm_get_device_status() returns.  The library keeps one small piece of
+ * per-device state (the status word and, for split-K launches, a workspace
+ * it allocates on first use); gemm_shutdown() frees it.
+ *
+ * Thread safety: calls may come from several host threads; each call only
+ * reads shared configuration.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+/* The library is built with hidden visibility; only these are exported. */
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,        /* negative size, unknown enum, bad key */
+    GEMM_ERR_NULLPTR = -2,            /* a matrix that must be read/written is NULL */
+    GEMM_ERR_BAD_LD = -3,             /* lda < max(1,K), ldb < max(1,N) or ldc < max(1,N) */
+    GEMM_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3 */
+    GEMM_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed */
+    GEMM_ERR_DEVICE_TIMEOUT = -6,     /* a pipeline wait on the GPU ran out of time */
+    GEMM_ERR_ALIAS = -7,              /* C overlaps A or B */
+    GEMM_ERR_TOO_LARGE = -8           /* a dimension or pitch exceeds 2^31 - 1 */
+} gemm_status_t;
+
+typedef enum {
+    GEMM_OUT_BF16 = 0,  /* C holds bf16 (uint16 bit patterns) */
+    GEMM_OUT_F32 = 1    /* C holds fp32 */
+} gemm_out_t;
+
+/*
+ * FP32 SGEMM: C = alpha * A * B + beta * C, all fp32, on the CUDA cores.
+ * Source: "CUDA hand-written SGEMM: 0.4 -> 10.23 TFLOPS" (gtnt.cn),
+ * section 1.1 (C = A*B, row-major) generalised by "Blackwell BF16 GEMM ..."
+ * section 1.1 (alpha, beta).
+ *   M, N, K     sizes, >= 0
+ *   A, lda      device fp32, M x K, pitch lda
+ *   B, ldb      device fp32, K x N, pitch ldb
+ *   C, ldc      device fp32, M x N, pitch ldc; read only if beta != 0
+ *   stream      cudaStream_t to enqueue on
+ * Returns GEMM_OK or a gemm_status_t error; on error nothing is launched.
+ */
+GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha,
+             const float *A, int64_t lda, const float *B, int64_t ldb,
+             float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * BF16 GEMM with FP32 accumulation on the tcgen05 tensor cores:
+ * C = alpha * A * B + beta * C, accumulated in fp32, alpha/beta applied in
+ * fp32, then stored as bf16 (round to nearest even) or fp32.
+ * Source: "Blackwell BF16 GEMM ..." (lshu.cn), sections 1.1-1.2 (operation,
+ * bf16 format, fp32 accumulation), 2.2-2.3 (TMA-fed asynchronous pipeline),
+ * 4.3 and 6.2 (tails), 6.3 (the accumulator must be fp32).
+ *   A, lda      device bf16 (uint16 bits), M x K, pitch lda
+ *   B, ldb      device bf16 (uint16 bits), K x N, pitch ldb
+ *   C, ldc      device, M x N, pitch ldc, element type c_type; it is both
+ *               the beta input and the output
+ *   c_type      GEMM_OUT_BF16 or GEMM_OUT_F32
+ * Returns GEMM_OK or a gemm_status_t error; on error nothing is launched.
+ */
+GEMM_API int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
+              const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+              float beta, void *C, int64_t ldc, int c_type, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's
+ * pipeline status: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a kernel since the
+ * last call gave up on a wait (its output is then incomplete).  Returns
+ * GEMM_ERR_CUDA if the synchronisation itself failed.
+ */
+GEMM_API int gemm_get_device_status(void *stream);
+
+/*
+ * Details of the last recorded device fault (0 if none): bits 0-7 the role
+ * (1 producer, 2 MMA issuer, 3 epilogue), bits 8-15 the pipeline stage,
+ * bits 16-47 the tile index.  Does not clear it.
+ */
+GEMM_API int64_t gemm_get_device_fault_info(void);
+
+/* A static, human-readable name for a gemm_status_t. */
+GEMM_API const char *gemm_status_string(int status);
+
+/*
+ * Tuning and debugging knobs (process-wide).  Keys:
+ *   "watchdog_ms"   time limit of one pipeline wait on the GPU, ms (default 2000)
+ *   "force_path"    0 auto, 1 force the generic (non-TMA) kernels,
+ *                   2 force the tcgen05 kernel (fails on misaligned input)
+ *   "fault_inject"  1: the next tcgen05 launch withholds one pipeline stage so
+ *                   its waits run out (tests the watchdog); resets itself
+ *   "split_k"       0 auto, else the number of K slices for the tcgen05 kernel
+ *   "bf16_tile_n"   0 auto, else 128 or 256 (tcgen05 tile width)
+ * Returns GEMM_OK or GEMM_ERR_INVALID_ARG for an unknown key or value.
+ */
+GEMM_API int gemm_set_config(const char *key, int64_t value);
+GEMM_API int gemm_get_config(const char *key, int64_t *value);
+
+/*
+ * Name of the kernel the last successful gemm_* call on this host thread
+ * launched ("sgemm_simt", "bf16_tcgen05", "bf16_simt", "scale_c", "none").
+ */
+GEMM_API const char *gemm_last_kernel(void);
+
+/* Frees the per-device state of the current device.  Safe to call twice. */
+GEMM_API int gemm_shutdown(void);
+
+/* Library ABI version, currently 1. */
+GEMM_API int gemm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

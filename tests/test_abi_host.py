@@ -1,0 +1,128 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function the public header declares, and rejects bad
+arguments before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_gemm_02_gb300 import _build, binding
+
+    _build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:GEMM_API\s+)?(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(gemm_[a-z0-9_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("gemm_f32", "gemm_bf16", "gemm_get_device_status", "gemm_status_string",
+                 "gemm_set_config", "gemm_shutdown"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from dense_gemm_02_gb300 import binding
+
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+        assert name in binding.SIGNATURES, f"{name} has no binding signature"
+
+
+def test_only_declared_symbols_are_exported(lib):
+    # The library is built with hidden visibility; its dynamic symbol table
+    # should hold the C ABI and nothing else of ours.
+    import subprocess
+
+    from dense_gemm_02_gb300 import _build
+
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True)
+    if out.returncode != 0:
+        pytest.skip("nm unavailable")
+    ours = {ln.split()[-1] for ln in out.stdout.splitlines() if " T gemm_" in ln}
+    assert ours == set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    from dense_gemm_02_gb300 import binding as b
+
+    assert b.abi_version() == 1
+    for code in range(-8, 1):
+        assert b.status_string(code).startswith("GEMM_")
+    assert "unknown" in b.status_string(42)
+
+
+def test_argument_errors_are_reported_before_any_cuda_call(lib):
+    from dense_gemm_02_gb300 import binding as b
+
+    f = b.gemm_f32
+    fake = 1 << 20  # never dereferenced: every call below fails validation
+    assert f(-1, 4, 4, 1.0, fake, 4, fake, 4, 0.0, fake, 4, None) == b.GEMM_ERR_INVALID_ARG
+    assert f(4, 4, 4, 1.0, fake, 3, fake, 4, 0.0, fake, 4, None) == b.GEMM_ERR_BAD_LD
+    assert f(4, 4, 4, 1.0, fake, 4, fake, 3, 0.0, fake, 4, None) == b.GEMM_ERR_BAD_LD
+    assert f(4, 4, 4, 1.0, fake, 4, fake, 4, 0.0, fake, 3, None) == b.GEMM_ERR_BAD_LD
+    assert f(4, 4, 4, 1.0, None, 4, fake, 4, 0.0, fake + 4096, 4, None) == b.GEMM_ERR_NULLPTR
+    assert f(4, 4, 4, 1.0, fake, 4, fake + 4096, 4, 0.0, None, 4, None) == b.GEMM_ERR_NULLPTR
+    assert f(1 << 31, 4, 4, 1.0, fake, 4, fake, 4, 0.0, fake, 4, None) == b.GEMM_ERR_TOO_LARGE
+    # C overlapping A or B
+    assert f(4, 4, 4, 1.0, fake, 4, fake + 4096, 4, 0.0, fake + 16, 4, None) == b.GEMM_ERR_ALIAS
+    assert f(4, 4, 4, 1.0, fake, 4, fake + 4096, 4, 0.0, fake + 4096 + 60, 4,
+             None) == b.GEMM_ERR_ALIAS
+    # empty problems are a no-op with no pointer needed
+    assert f(0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, None) == b.GEMM_OK
+    assert f(4, 0, 4, 1.0, None, 4, None, 1, 0.0, None, 1, None) == b.GEMM_OK
+    g = b.gemm_bf16
+    assert g(4, 4, 4, 1.0, fake, 4, fake, 4, 0.0, fake, 4, 7, None) == b.GEMM_ERR_INVALID_ARG
+    assert g(4, 4, 4, 1.0, fake, 2, fake, 4, 0.0, fake, 4, 0, None) == b.GEMM_ERR_BAD_LD
+    assert g(4, 4, 4, 1.0, fake, 4, fake + 4096, 4, 0.0, fake + 8, 4, 1,
+             None) == b.GEMM_ERR_ALIAS
+
+
+def test_config_keys(lib):
+    from dense_gemm_02_gb300 import binding as b
+
+    old = b.get_config("watchdog_ms")
+    b.set_config("watchdog_ms", 250)
+    assert b.get_config("watchdog_ms") == 250
+    b.set_config("watchdog_ms", old)
+    with pytest.raises(b.GemmError):
+        b.set_config("no_such_key", 1)
+    with pytest.raises(b.GemmError):
+        b.set_config("bf16_tile_n", 96)
+    assert b.last_kernel() in {"none", "sgemm_simt", "bf16_tcgen05", "bf16_simt", "scale_c"}
+
+
+def test_package_fails_loudly_without_library(tmp_path, monkeypatch):
+    from dense_gemm_02_gb300 import _build, binding
+
+    monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.lib()
+
+
+def test_ctypes_signatures_match_header_arity(lib):
+    from dense_gemm_02_gb300 import binding
+
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    for name, (_res, args) in binding.SIGNATURES.items():
+        m = re.search(name + r"\s*\(([^)]*)\)", text)
+        assert m, name
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(params) == len(args), name
+    assert isinstance(lib, ctypes.CDLL)
