@@ -23,6 +23,7 @@ GEMM_ERR_CUDA = -5
 GEMM_ERR_DEVICE_TIMEOUT = -6
 GEMM_ERR_ALIAS = -7
 GEMM_ERR_TOO_LARGE = -8
+GEMM_ERR_SCRATCH_LIMIT = -9
 
 GEMM_OUT_BF16 = 0
 GEMM_OUT_F32 = 1
@@ -34,6 +35,8 @@ SIGNATURES = {
     "gemm_f32": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]),
     "gemm_bf16": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _int,
                          _vp]),
+    "gemm_bf16_noalloc": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
+                                 _int, _vp]),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_get_device_fault_info": (_i64, []),
     "gemm_status_string": (_cp, [_int]),
@@ -99,6 +102,12 @@ def gemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream) -> int:
 def gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream) -> int:
     """Raw call; A/B/C are device addresses, c_type GEMM_OUT_BF16/F32."""
     return lib().gemm_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream)
+
+
+def gemm_bf16_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream) -> int:
+    """Raw call of the allocation-free variant (split-K scratch in a static
+    device array); same arguments as gemm_bf16."""
+    return lib().gemm_bf16_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream)
 
 
 def get_device_status(stream=None) -> int:

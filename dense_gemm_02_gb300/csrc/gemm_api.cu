@@ -40,11 +40,11 @@ size_t span_bytes(int64_t rows, int64_t cols, int64_t ld, size_t esz) {
     return (size_t)((rows - 1) * ld + cols) * esz;
 }
 
-// Checks shared by both entry points.  Returns GEMM_OK, an error, or 1 for
-// "valid, nothing to do".
-int validate(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
-             size_t a_esz, const void *B, int64_t ldb, size_t b_esz, float beta, const void *C,
-             int64_t ldc, size_t c_esz) {
+}  // namespace
+
+int validate_gemm_args(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                       size_t a_esz, const void *B, int64_t ldb, size_t b_esz, float beta,
+                       const void *C, int64_t ldc, size_t c_esz) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim || lda > kMaxDim || ldb > kMaxDim ||
         ldc > kMaxDim)
@@ -64,8 +64,6 @@ int validate(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_
     (void)beta;
     return GEMM_OK;
 }
-
-}  // namespace
 
 int device_state(DeviceState **out) {
     int dev = -1;
@@ -136,7 +134,7 @@ using namespace gemm;
 extern "C" int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                         int64_t lda, const float *B, int64_t ldb, float beta, float *C,
                         int64_t ldc, void *stream) {
-    int rc = validate(M, N, K, alpha, A, lda, 4, B, ldb, 4, beta, C, ldc, 4);
+    int rc = validate_gemm_args(M, N, K, alpha, A, lda, 4, B, ldb, 4, beta, C, ldc, 4);
     if (rc == 1) {
         set_last_kernel("none");
         return GEMM_OK;
@@ -161,7 +159,7 @@ extern "C" int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uin
                          int64_t ldc, int c_type, void *stream) {
     if (c_type != GEMM_OUT_BF16 && c_type != GEMM_OUT_F32) return GEMM_ERR_INVALID_ARG;
     const bool c_f32 = (c_type == GEMM_OUT_F32);
-    int rc = validate(M, N, K, alpha, A, lda, 2, B, ldb, 2, beta, C, ldc, c_f32 ? 4 : 2);
+    int rc = validate_gemm_args(M, N, K, alpha, A, lda, 2, B, ldb, 2, beta, C, ldc, c_f32 ? 4 : 2);
     if (rc == 1) {
         set_last_kernel("none");
         return GEMM_OK;
@@ -234,6 +232,8 @@ extern "C" const char *gemm_status_string(int status) {
             return "GEMM_ERR_DEVICE_TIMEOUT: a GPU pipeline wait ran out of time";
         case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS: C overlaps A or B";
         case GEMM_ERR_TOO_LARGE: return "GEMM_ERR_TOO_LARGE: dimension exceeds 2^31-1";
+        case GEMM_ERR_SCRATCH_LIMIT:
+            return "GEMM_ERR_SCRATCH_LIMIT: needs more split-K scratch than the static maximum";
         default: return "unknown gemm status";
     }
 }

@@ -482,16 +482,19 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Exactly one of st (library-owned workspace, grown on demand) and ext
+// (caller-provided scratch, never allocated) supplies the split-K storage.
 template <int BN>
-int launch_tc(DeviceState *st, TcParams &p, const uint16_t *A, int64_t lda, const uint16_t *B,
-              int64_t ldb, cudaStream_t stream) {
+int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *ext,
+              TcParams &p, const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+              cudaStream_t stream) {
     using Cfg = TcCfg<BN>;
     static bool attr_done[kMaxDevices] = {};
-    if (!attr_done[st->device]) {
+    if (!attr_done[device]) {
         if (cudaFuncSetAttribute(bf16_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_ALLOC) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        attr_done[st->device] = true;
+        attr_done[device] = true;
     }
     alignas(64) CUtensorMap ta, tb;
     if (!make_map(&ta, A, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)lda, TC_BK, TC_BM))
@@ -507,8 +510,8 @@ int launch_tc(DeviceState *st, TcParams &p, const uint16_t *A, int64_t lda, cons
     const RuntimeConfig cfg = runtime_config();
     if (cfg.split_k > 0) {
         splits = (int)cfg.split_k;
-    } else if (tiles * 2 <= st->sm_count && p.num_kb >= 8) {
-        splits = (int)(st->sm_count / tiles);
+    } else if (tiles * 2 <= sm_count && p.num_kb >= 8) {
+        splits = (int)(sm_count / tiles);
         if (splits > p.num_kb / 4) splits = p.num_kb / 4;
     }
     if (splits < 1) splits = 1;
@@ -522,21 +525,36 @@ int launch_tc(DeviceState *st, TcParams &p, const uint16_t *A, int64_t lda, cons
     p.counters = nullptr;
     if (p.splits > 1) {
         const size_t ws_bytes = (size_t)units * TC_BM * BN * sizeof(float);
-        const int rc = ensure_splitk_workspace(st, ws_bytes, (size_t)tiles);
-        if (rc != GEMM_OK) return rc;
-        p.ws = st->splitk_ws;
-        p.counters = st->splitk_counters;
+        if (ext) {
+            if (ws_bytes > ext->ws_bytes || (size_t)tiles > ext->counters_n)
+                return GEMM_ERR_SCRATCH_LIMIT;
+            // The counters must start at zero; a call that gave up earlier
+            // may have left some mid-count.
+            if (cudaMemsetAsync(ext->counters, 0, (size_t)tiles * sizeof(unsigned), stream) !=
+                cudaSuccess)
+                return GEMM_ERR_CUDA;
+            p.ws = ext->ws;
+            p.counters = ext->counters;
+        } else {
+            const int rc = ensure_splitk_workspace(st, ws_bytes, (size_t)tiles);
+            if (rc != GEMM_OK) return rc;
+            p.ws = st->splitk_ws;
+            p.counters = st->splitk_counters;
+        }
     }
-    const int grid = (int)(units < st->sm_count ? units : st->sm_count);
+    const int grid = (int)(units < sm_count ? units : sm_count);
     bf16_tc_kernel<BN><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_bf16_tcgen05(DeviceState *st, int M, int N, int K, float alpha, const uint16_t *A,
-                        int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,
-                        int64_t ldc, bool c_f32, cudaStream_t stream) {
+namespace {
+
+int launch_common(int device, int sm_count, DeviceState *st, const ExternalScratch *ext,
+                  unsigned long long *fault_word, int M, int N, int K, float alpha,
+                  const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, float beta,
+                  void *C, int64_t ldc, bool c_f32, cudaStream_t stream) {
     TcParams p{};
     p.M = M;
     p.N = N;
@@ -548,15 +566,32 @@ int launch_bf16_tcgen05(DeviceState *st, int M, int N, int K, float alpha, const
     p.c_f32 = c_f32 ? 1 : 0;
     const int esz = c_f32 ? 4 : 2;
     p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && ((ldc * esz) % 16 == 0);
-    p.fault_word = st->fault_word;
+    p.fault_word = fault_word;
     const RuntimeConfig cfg = runtime_config();
     p.timeout_ns = (unsigned long long)cfg.watchdog_ms * 1000000ull;
     p.fault_inject = cfg.fault_inject ? 1 : 0;
     if (p.fault_inject) consume_fault_inject();
     int bn = (int)cfg.bf16_tile_n;
     if (bn != 128 && bn != 256) bn = (N <= 128) ? 128 : 256;
-    return bn == 256 ? launch_tc<256>(st, p, A, lda, B, ldb, stream)
-                     : launch_tc<128>(st, p, A, lda, B, ldb, stream);
+    return bn == 256 ? launch_tc<256>(device, sm_count, st, ext, p, A, lda, B, ldb, stream)
+                     : launch_tc<128>(device, sm_count, st, ext, p, A, lda, B, ldb, stream);
+}
+
+}  // namespace
+
+int launch_bf16_tcgen05(DeviceState *st, int M, int N, int K, float alpha, const uint16_t *A,
+                        int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,
+                        int64_t ldc, bool c_f32, cudaStream_t stream) {
+    return launch_common(st->device, st->sm_count, st, nullptr, st->fault_word, M, N, K, alpha,
+                         A, lda, B, ldb, beta, C, ldc, c_f32, stream);
+}
+
+int launch_bf16_tcgen05_external(int device, int sm_count, const ExternalScratch &ext, int M,
+                                 int N, int K, float alpha, const uint16_t *A, int64_t lda,
+                                 const uint16_t *B, int64_t ldb, float beta, void *C,
+                                 int64_t ldc, bool c_f32, cudaStream_t stream) {
+    return launch_common(device, sm_count, nullptr, &ext, ext.fault_word, M, N, K, alpha, A, lda,
+                         B, ldb, beta, C, ldc, c_f32, stream);
 }
 
 }  // namespace gemm

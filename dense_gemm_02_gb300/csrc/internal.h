@@ -87,6 +87,28 @@ cudaError_t launch_gemm_simt_generic(int M, int N, int K, float alpha, const voi
 cudaError_t launch_scale_c(int M, int N, float beta, void *C, int64_t ldc, bool c_f32,
                            cudaStream_t stream);
 
+// Host-side argument checks shared by the entry points.  Returns GEMM_OK,
+// an error, or 1 for "valid, nothing to do" (M == 0 or N == 0).
+int validate_gemm_args(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
+                       size_t a_esz, const void *B, int64_t ldb, size_t b_esz, float beta,
+                       const void *C, int64_t ldc, size_t c_esz);
+
+// Split-K storage supplied by the caller instead of the library workspace.
+struct ExternalScratch {
+    float *ws;                       // fp32 partial tiles
+    size_t ws_bytes;
+    unsigned *counters;              // one per output tile; cleared before each launch
+    size_t counters_n;
+    unsigned long long *fault_word;  // pipeline fault record
+};
+
+// Same kernel as launch_bf16_tcgen05 with split-K storage from `ext`; never
+// allocates.  GEMM_ERR_SCRATCH_LIMIT if the chosen split needs more.
+int launch_bf16_tcgen05_external(int device, int sm_count, const ExternalScratch &ext, int M,
+                                 int N, int K, float alpha, const uint16_t *A, int64_t lda,
+                                 const uint16_t *B, int64_t ldb, float beta, void *C,
+                                 int64_t ldc, bool c_f32, cudaStream_t stream);
+
 // BF16 tcgen05 GEMM.  Requires 16-byte aligned A/B bases and lda, ldb
 // multiples of 8.  Returns a gemm_status_t.
 int launch_bf16_tcgen05(DeviceState *st, int M, int N, int K, float alpha, const uint16_t *A,

@@ -71,7 +71,9 @@ typedef enum {
     GEMM_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed */
     GEMM_ERR_DEVICE_TIMEOUT = -6,     /* a pipeline wait on the GPU ran out of time */
     GEMM_ERR_ALIAS = -7,              /* C overlaps A or B */
-    GEMM_ERR_TOO_LARGE = -8           /* a dimension or pitch exceeds 2^31 - 1 */
+    GEMM_ERR_TOO_LARGE = -8,          /* a dimension or pitch exceeds 2^31 - 1 */
+    GEMM_ERR_SCRATCH_LIMIT = -9       /* gemm_bf16_noalloc: the call needs more split-K
+                                         scratch than its static maximum */
 } gemm_status_t;
 
 typedef enum {
@@ -112,6 +114,44 @@ GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha,
 GEMM_API int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
               const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
               float beta, void *C, int64_t ldc, int c_type, void *stream);
+
+/*
+ * Allocation-free BF16 GEMM.  The source pages have no counterpart: this is
+ * an interface for callers that cannot call cudaMalloc at all, for example
+ * code that runs inside a host whose device memory is fully owned by its own
+ * arena or caching allocator (a plugin, a framework extension) and may not
+ * allocate around it, or latency-critical code that cannot accept the
+ * implicit device synchronisation an allocation can cause.
+ *
+ * Same operation, arguments, layout and results as gemm_bf16 (same kernel,
+ * same split choice), except that the split-K scratch lives in a statically
+ * sized device array compiled into the library instead of a workspace the
+ * library allocates:
+ *   - the array holds GEMM_NOALLOC_SCRATCH_BYTES (32 MiB) and is reserved on
+ *     every GPU that loads its module, until the process exits;
+ *   - a call whose split-K partials need more than the array offers (at
+ *     most 4096 output tiles and about 32 MiB of fp32 partials) returns
+ *     GEMM_ERR_SCRATCH_LIMIT and launches nothing; the automatic split
+ *     choice stays well inside the limit, a large forced "split_k" may not;
+ *   - A and B must be TMA-compatible (16-byte aligned bases, lda and ldb
+ *     multiples of 8), else GEMM_ERR_INVALID_ARG;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture on that device;
+ *   - every call shares the one array and clears the parts that must start
+ *     at zero (tile counters, fault record) on `stream` before its kernel;
+ *     calls whose executions overlap on the GPU (different streams, no
+ *     ordering between them) race on the array and give wrong results;
+ *   - a pipeline wait that runs out of time is recorded only in the array's
+ *     fault record (gemm_get_device_status does not see it); the kernel
+ *     still returns and leaves this call's output incomplete.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define GEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
+GEMM_API int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                               const uint16_t *A, int64_t lda, const uint16_t *B,
+                               int64_t ldb, float beta, void *C, int64_t ldc, int c_type,
+                               void *stream);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's
