@@ -20,6 +20,9 @@ std::atomic<int64_t> g_force_path{0};
 std::atomic<int64_t> g_fault_inject{0};
 std::atomic<int64_t> g_split_k{0};
 std::atomic<int64_t> g_bf16_tile_n{0};
+std::atomic<int64_t> g_tail_split_off{0};
+std::atomic<int64_t> g_raster_group{0};
+std::atomic<int64_t> g_cta_pair{0};
 std::atomic<int64_t> g_last_fault{0};
 
 std::mutex g_state_mu;
@@ -120,7 +123,8 @@ int ensure_splitk_workspace(DeviceState *st, size_t ws_bytes, size_t n_counters)
 
 RuntimeConfig runtime_config() {
     return RuntimeConfig{g_watchdog_ms.load(), g_force_path.load(), g_fault_inject.load(),
-                         g_split_k.load(), g_bf16_tile_n.load()};
+                         g_split_k.load(),      g_bf16_tile_n.load(), g_tail_split_off.load(),
+                         g_raster_group.load(), g_cta_pair.load()};
 }
 
 void consume_fault_inject() { g_fault_inject.store(0); }
@@ -255,6 +259,15 @@ extern "C" int gemm_set_config(const char *key, int64_t value) {
     } else if (!strcmp(key, "bf16_tile_n")) {
         if (value != 0 && value != 128 && value != 256) return GEMM_ERR_INVALID_ARG;
         g_bf16_tile_n.store(value);
+    } else if (!strcmp(key, "tail_split_off")) {
+        if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+        g_tail_split_off.store(value);
+    } else if (!strcmp(key, "raster_group")) {
+        if (value < 0 || value > 1024) return GEMM_ERR_INVALID_ARG;
+        g_raster_group.store(value);
+    } else if (!strcmp(key, "cta_pair")) {
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+        g_cta_pair.store(value);
     } else {
         return GEMM_ERR_INVALID_ARG;
     }
@@ -268,6 +281,9 @@ extern "C" int gemm_get_config(const char *key, int64_t *value) {
     else if (!strcmp(key, "fault_inject")) *value = g_fault_inject.load();
     else if (!strcmp(key, "split_k")) *value = g_split_k.load();
     else if (!strcmp(key, "bf16_tile_n")) *value = g_bf16_tile_n.load();
+    else if (!strcmp(key, "tail_split_off")) *value = g_tail_split_off.load();
+    else if (!strcmp(key, "raster_group")) *value = g_raster_group.load();
+    else if (!strcmp(key, "cta_pair")) *value = g_cta_pair.load();
     else return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }

@@ -35,6 +35,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -51,6 +52,10 @@ constexpr int TC_UMMA_K = 16;        // K of one kind::f16 MMA
 constexpr int TC_THREADS = 192;      // 6 warps
 constexpr int TC_EPI_THREADS = 128;  // warps 2-5
 constexpr int TC_EPI_BAR = 1;        // named barrier id of the epilogue warps
+// Epilogue staging for TMA stores: each epilogue warp owns two 4 KiB
+// buffers (a 32 x 32 fp32 or bf16 chunk of C, swizzled), 1024-byte aligned.
+constexpr int kEpiChunkBytes = 4096;
+constexpr int kEpiStagingBytes = 4 * 2 * kEpiChunkBytes;
 
 template <int BN>
 struct TcCfg {
@@ -58,10 +63,9 @@ struct TcCfg {
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KiB
     static constexpr int B_BYTES = BN * TC_BK * 2;     // 32 KiB at BN = 256
     static constexpr int B_BOX_BYTES = 64 * TC_BK * 2; // one 64-column B box, 8 KiB
-    static constexpr int STAGE_TX = A_BYTES + B_BYTES;
-    static constexpr int B_BOXES = BN / 64;
     static constexpr int OFF_B = STAGES * A_BYTES;
-    static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_STAGE = OFF_B + STAGES * B_BYTES;  // epilogue staging
+    static constexpr int OFF_BAR = OFF_STAGE + kEpiStagingBytes;
     static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -76,11 +80,15 @@ struct TcParams {
     int num_m_blk, num_n_blk, num_kb;
     int splits, kb_per_split;
     int num_units;
+    int group_m;     // M-blocks per raster band
+    int tiles_main;  // tiles run at full width; the rest are split along N
+    int tail_split;  // sub-tiles per tail tile (1, 2 or 4)
     float alpha, beta;
     void *C;
     long long ldc;
     int c_f32;
     int c_vec;
+    int c_tma;  // C is written by TMA stores through shared memory
     float *ws;
     unsigned *counters;
     unsigned long long *fault_word;
@@ -102,19 +110,44 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A bf16 (7-9 = 1), B bf16 (10-12 = 1), A K-major (bit 15 = 0), B MN-major
 // (bit 16 = 1, B is row-major K x N), N >> 3 in bits 17-22, M >> 4 in 24-28.
-template <int BN>
-__host__ __device__ constexpr uint32_t idesc_bf16_f32() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(BN >> 3) << 17) |
-           ((uint32_t)(TC_BM >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, int m = TC_BM) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void decode_unit(const TcParams &p, int u, int &tile, int &m_blk,
-                                            int &n_blk, int &kb0, int &kb1) {
-    tile = u / p.splits;
-    const int split = u - tile * p.splits;
-    grouped_tile_coords(tile, p.num_m_blk, p.num_n_blk, m_blk, n_blk);
-    kb0 = split * p.kb_per_split;
-    kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+// One unit of work: output rows m_blk*128.., columns n0..n0+width-1, K
+// blocks kb0..kb1-1.  `tile` indexes the full-width tile (split-K counters).
+struct Unit {
+    int tile, m_blk, n0, width, kb0, kb1, split;
+};
+
+// Unit order: split-K launches enumerate (tile, slice); otherwise the first
+// tiles_main tiles run at full width BN and each remaining tile (the last,
+// partial wave of the persistent grid) is cut into tail_split narrower
+// sub-tiles so that the partial wave spreads over more SMs.
+template <int BN>
+__device__ __forceinline__ Unit decode_unit(const TcParams &p, int u) {
+    Unit r;
+    int sub = 0, nsub = 1;
+    r.split = 0;
+    if (p.splits > 1) {
+        r.tile = u / p.splits;
+        r.split = u - r.tile * p.splits;
+    } else if (u < p.tiles_main) {
+        r.tile = u;
+    } else {
+        const int v = u - p.tiles_main;
+        r.tile = p.tiles_main + v / p.tail_split;
+        sub = v - (v / p.tail_split) * p.tail_split;
+        nsub = p.tail_split;
+    }
+    int n_blk;
+    grouped_tile_coords(r.tile, p.num_m_blk, p.num_n_blk, p.group_m, r.m_blk, n_blk);
+    r.width = BN / nsub;
+    r.n0 = n_blk * BN + sub * r.width;
+    r.kb0 = r.split * p.kb_per_split;
+    r.kb1 = min(r.kb0 + p.kb_per_split, p.num_kb);
+    return r;
 }
 
 __device__ __forceinline__ void record_fault(const TcParams &p, volatile int *abort_flag,
@@ -200,10 +233,97 @@ __device__ __forceinline__ void store_row_chunk(const TcParams &p, int gm, int g
     }
 }
 
+// Writes columns gn..gn+31 of the warp's 32 rows (gm0..gm0+31; this thread's
+// row is gm0 + lane) as C = alpha * acc + beta * C through the warp's
+// staging buffers and a TMA store.  The staging layout is the one the C
+// tensor map's swizzle expects: fp32 rows of 128 bytes with 16-byte chunk c
+// at c ^ (row & 7); bf16 rows of 64 bytes with chunk c at c ^ ((row >> 1) & 3).
+// Stores are asynchronous; a buffer is reused once the store issued two
+// chunks earlier has finished reading it.
+__device__ __forceinline__ void store_chunk_tma(const TcParams &p, const CUtensorMap *tmC,
+                                                uint8_t *warp_stage, uint32_t &seq, int lane,
+                                                int gm0, int gn, const float (&acc)[32]) {
+    const int gm = gm0 + lane;
+    const float alpha = p.alpha, beta = p.beta;
+    float o[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = alpha * acc[j];
+    if (beta != 0.f && gm < p.M) {
+        if (p.c_f32) {
+            const float *crow = static_cast<const float *>(p.C) + (long long)gm * p.ldc + gn;
+            if (gn + 32 <= p.N) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 c = reinterpret_cast<const float4 *>(crow)[j];
+                    o[4 * j] = fmaf(alpha, acc[4 * j], beta * c.x);
+                    o[4 * j + 1] = fmaf(alpha, acc[4 * j + 1], beta * c.y);
+                    o[4 * j + 2] = fmaf(alpha, acc[4 * j + 2], beta * c.z);
+                    o[4 * j + 3] = fmaf(alpha, acc[4 * j + 3], beta * c.w);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (gn + j < p.N) o[j] = fmaf(alpha, acc[j], beta * crow[j]);
+            }
+        } else {
+            const uint16_t *crow = static_cast<const uint16_t *>(p.C) + (long long)gm * p.ldc + gn;
+            if (gn + 32 <= p.N) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 c = reinterpret_cast<const uint4 *>(crow)[j];
+                    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const uint32_t h = (e & 1) ? (cw[e >> 1] >> 16) : (cw[e >> 1] & 0xFFFFu);
+                        o[8 * j + e] = fmaf(alpha, acc[8 * j + e], beta * bf16_bits_to_float(h));
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (gn + j < p.N)
+                        o[j] = fmaf(alpha, acc[j], beta * bf16_bits_to_float(crow[j]));
+            }
+        }
+    }
+    uint8_t *buf = warp_stage + (seq & 1u) * kEpiChunkBytes;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    if (p.c_f32) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) * 16)) =
+                make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 pr = __floats2bfloat162_rn(o[8 * c + 2 * e], o[8 * c + 2 * e + 1]);
+                w[e] = *reinterpret_cast<uint32_t *>(&pr);
+            }
+            *reinterpret_cast<uint4 *>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) * 16)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) {
+        // A chunk wholly outside C stores nothing, but still closes a
+        // (then empty) group so that the buffer-reuse wait above always
+        // refers to the store issued two chunks earlier.
+        if (gm0 < p.M && gn < p.N) tma_store_2d(tmC, buf, gn, gm0);
+        bulk_commit_group();
+    }
+    ++seq;
+}
+
 template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     using Cfg = TcCfg<BN>;
     constexpr int S = Cfg::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -260,13 +380,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             int withheld = -1;
             bool ok = true;
             for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-                int tile, mb, nb, kb0, kb1;
-                decode_unit(p, u, tile, mb, nb, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const Unit w = decode_unit<BN>(p, u);
+                if (w.n0 >= p.N) continue;  // sub-tile wholly past the N edge
+                const int boxes = w.width / 64;
+                const uint32_t tx = Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) {
-                        record_fault(p, abort_flag, kRoleProducer, s, tile);
+                        record_fault(p, abort_flag, kRoleProducer, s, w.tile);
                         ok = false;
                         break;
                     }
@@ -274,12 +396,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         withheld = 0;  // test hook: this stage is never filled
                         continue;
                     }
-                    mbar_arrive_expect_tx(&full[s], Cfg::STAGE_TX);
-                    tma_load_2d(sA + s * Cfg::A_BYTES, &tmA, &full[s], kb * TC_BK, mb * TC_BM);
-#pragma unroll
-                    for (int j = 0; j < Cfg::B_BOXES; ++j)
+                    mbar_arrive_expect_tx(&full[s], tx);
+                    tma_load_2d(sA + s * Cfg::A_BYTES, &tmA, &full[s], kb * TC_BK,
+                                w.m_blk * TC_BM);
+                    for (int j = 0; j < boxes; ++j)
                         tma_load_2d(sB + s * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES, &tmB, &full[s],
-                                    nb * BN + j * 64, kb * TC_BK);
+                                    w.n0 + j * 64, kb * TC_BK);
                 }
             }
             // Let every copy started here land before the CTA can exit.
@@ -293,26 +415,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_bf16_f32<BN>();
             const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
             uint32_t it = 0, local = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++local) {
-                int tile, mb, nb, kb0, kb1;
-                decode_unit(p, u, tile, mb, nb, kb0, kb1);
+            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+                const Unit w = decode_unit<BN>(p, u);
+                if (w.n0 >= p.N) continue;
+                const uint32_t idesc = idesc_bf16_f32(w.width);
                 const uint32_t b = local & 1u, use = local >> 1;
+                ++local;
                 if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
-                    record_fault(p, abort_flag, kRoleMma, 0xfe, tile);
+                    record_fault(p, abort_flag, kRoleMma, 0xfe, w.tile);
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
                     const int s = it % S;
                     const uint32_t ph = (it / S) & 1u;
                     if (!mbar_wait(&full[s], ph, abort_flag, p.timeout_ns)) {
-                        record_fault(p, abort_flag, kRoleMma, s, tile);
+                        record_fault(p, abort_flag, kRoleMma, s, w.tile);
                         ok = false;
                         break;
                     }
@@ -328,7 +451,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         // 8 K-rows 1024 bytes apart; a K step of 16 is 16 rows.
                         const uint64_t bd =
                             smem_desc_sw128(sb + k * 16 * 128, Cfg::B_BOX_BYTES, 1024);
-                        umma_f16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                        umma_f16(d_tmem, ad, bd, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit(&empty[s]);  // frees the stage once these MMAs finish
                 }
@@ -345,11 +468,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;
         const int et = threadIdx.x - 64;
+        uint8_t *warp_stage = smem + Cfg::OFF_STAGE + q * 2 * kEpiChunkBytes;
+        uint32_t stage_seq = 0;
         uint32_t local = 0;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++local) {
-            int tile, mb, nb, kb0, kb1;
-            decode_unit(p, u, tile, mb, nb, kb0, kb1);
+        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+            const Unit w = decode_unit<BN>(p, u);
+            if (w.n0 >= p.N) continue;
+            const int tile = w.tile;
             const uint32_t b = local & 1u, use = local >> 1;
+            ++local;
             // One thread waits (bounded) and the decision is shared, so the
             // epilogue warps always leave the loop together.
             if (et == 0) {
@@ -362,23 +489,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_wait(&tfull[b], use & 1u, abort_flag, p.timeout_ns, true);  // completed: no wait
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
-            const int gm = mb * TC_BM + row;
-            const int gn0 = nb * BN;
+            const int gm = w.m_blk * TC_BM + row;
+            const int gn0 = w.n0;
             if (p.splits == 1) {
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < w.width / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + c * 32, r);
                     tmem_ld_wait();
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    store_row_chunk(p, gm, gn0 + c * 32, v);
+                    if (p.c_tma)
+                        store_chunk_tma(p, &tmC, warp_stage, stage_seq, lane, gm - lane,
+                                        gn0 + c * 32, v);
+                    else
+                        store_row_chunk(p, gm, gn0 + c * 32, v);
                 }
                 tc_fence_before_sync();
                 mbar_arrive(&tempty[b]);
             } else {
-                const int split = u - tile * p.splits;
+                const int split = w.split;
                 float *wrow = p.ws + (((size_t)tile * p.splits + split) * TC_BM + row) * BN;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
@@ -441,11 +572,250 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
     }
 
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores of C have landed
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
+
+// ================================================================ CTA pairs
+//
+// The same GEMM with two CTAs (one per SM, a 2-CTA cluster) sharing each
+// tcgen05 MMA (cta_group::2): a 256 x BN output tile per pair, CTA r owning
+// rows r*128..r*128+127.  Each CTA loads its own 128 rows of A and its own
+// half of the tile's B columns; the even CTA's lane issues MMA M = 256, N =
+// BN that reads both CTAs' shared memory and writes both CTAs' TMEM.  Per
+// CTA a stage is 32 KiB instead of 48 KiB (B is split between the pair), so
+// six stages fit and L2 traffic per flop drops by a third.
+//
+//   full[s]   (even CTA only) 1 arrival (its producer, expect_tx = both CTAs'
+//             bytes) + the TMA bytes of both CTAs (TMA .cta_group::2 signals
+//             the even CTA's barrier)
+//   empty[s]  (each CTA) arrived by the MMA commit, multicast to both CTAs
+//   tfull[b]  (each CTA) arrived by the MMA commit, multicast
+//   tempty[b] (even CTA) 8 arrivals: one per epilogue warp of both CTAs
+struct Tc2Cfg {
+    static constexpr int BN = 256;                     // pair tile width
+    static constexpr int STAGES = 6;
+    static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // this CTA's 128 rows, 16 KiB
+    static constexpr int B_BOX_BYTES = 64 * TC_BK * 2; // 8 KiB
+    static constexpr int B_BYTES = 2 * B_BOX_BYTES;    // this CTA's half of 256 columns
+    static constexpr int OFF_B = STAGES * A_BYTES;
+    static constexpr int OFF_STAGE = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_BAR = OFF_STAGE + kEpiStagingBytes;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_ALLOC = SMEM_USED + 1024;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int EPI_WARPS_PER_PAIR = 8;
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    bf16_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+    using Cfg = Tc2Cfg;
+    constexpr int S = Cfg::STAGES;
+    constexpr int BN = Cfg::BN;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + Cfg::OFF_B;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + S;
+    uint64_t *tfull = bars + 2 * S;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
+    uint32_t *tmem_slot = misc;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    volatile int *epi_ok = reinterpret_cast<volatile int *>(misc + 3);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
+    const int pair = (int)cluster_id_x();
+    const int npairs = (int)num_clusters_x();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], Cfg::EPI_WARPS_PER_PAIR);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *epi_ok = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // the peer's barriers are initialised before any remote signal
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t it = 0;
+            int withheld = -1;
+            bool ok = true;
+            for (int u = pair; u < p.num_units && ok; u += npairs) {
+                const Unit w = decode_unit<BN>(p, u);
+                if (w.n0 >= p.N) continue;
+                const int half = w.width / 2;         // this CTA's B columns
+                const int boxes = half / 64;
+                const uint32_t tx = 2u * (Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES);
+                const int row0 = w.m_blk * 2 * TC_BM + (int)rank * TC_BM;
+                const int col0 = w.n0 + (int)rank * half;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1u;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) {
+                        record_fault(p, abort_flag, kRoleProducer, s, w.tile);
+                        ok = false;
+                        break;
+                    }
+                    if (p.fault_inject && pair == 0 && leader && it == 0) {
+                        withheld = 0;  // test hook: the stage's barrier never completes
+                        continue;
+                    }
+                    const uint32_t full_cl = mapa_shared(smem_addr(&full[s]), 0);
+                    if (leader) mbar_arrive_expect_tx(&full[s], tx);
+                    tma_load_2d_pair(sA + s * Cfg::A_BYTES, &tmA, full_cl, kb * TC_BK, row0);
+                    for (int j = 0; j < boxes; ++j)
+                        tma_load_2d_pair(sB + s * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES, &tmB,
+                                         full_cl, col0 + j * 64, kb * TC_BK);
+                }
+            }
+            // The even CTA's full barriers count both CTAs' copies: wait for
+            // the ones still in flight before the pair may exit.
+            if (leader) {
+                const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+                for (uint32_t i = first; i < it; ++i) {
+                    if ((int)i == withheld) continue;
+                    mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && leader) {
+            const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
+            uint32_t it = 0, local = 0;
+            bool ok = true;
+            for (int u = pair; u < p.num_units && ok; u += npairs) {
+                const Unit w = decode_unit<BN>(p, u);
+                if (w.n0 >= p.N) continue;
+                const uint32_t idesc = idesc_bf16_f32(w.width, 2 * TC_BM);
+                const uint32_t b = local & 1u, use = local >> 1;
+                ++local;
+                if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
+                    record_fault(p, abort_flag, kRoleMma, 0xfe, w.tile);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * BN;
+                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+                    const int s = it % S;
+                    const uint32_t ph = (it / S) & 1u;
+                    if (!mbar_wait(&full[s], ph, abort_flag, p.timeout_ns)) {
+                        record_fault(p, abort_flag, kRoleMma, s, w.tile);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t sa = a_base + s * Cfg::A_BYTES;
+                    const uint32_t sb = b_base + s * Cfg::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < TC_BK / TC_UMMA_K; ++k) {
+                        const uint64_t ad = smem_desc_sw128(sa + k * 32, 16, 1024);
+                        const uint64_t bd =
+                            smem_desc_sw128(sb + k * 16 * 128, Cfg::B_BOX_BYTES, 1024);
+                        umma_f16_pair(d_tmem, ad, bd, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair(&empty[s], 0x3);  // frees stage s in both CTAs
+                }
+                if (!ok) break;
+                umma_commit_pair(&tfull[b], 0x3);  // accumulator b complete in both CTAs
+            }
+            umma_commit_pair(drain, 0x1);
+            mbar_wait(drain, 0, abort_flag, p.timeout_ns, true);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue warps 2-5 (both CTAs)
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int et = threadIdx.x - 64;
+        uint8_t *warp_stage = smem + Cfg::OFF_STAGE + q * 2 * kEpiChunkBytes;
+        uint32_t stage_seq = 0;
+        const uint32_t tempty_cl0 = mapa_shared(smem_addr(&tempty[0]), 0);
+        const uint32_t tempty_cl1 = mapa_shared(smem_addr(&tempty[1]), 0);
+        uint32_t local = 0;
+        for (int u = pair; u < p.num_units; u += npairs) {
+            const Unit w = decode_unit<BN>(p, u);
+            if (w.n0 >= p.N) continue;
+            const uint32_t b = local & 1u, use = local >> 1;
+            ++local;
+            if (et == 0) {
+                const bool ok = mbar_wait(&tfull[b], use & 1u, abort_flag, p.timeout_ns);
+                if (!ok) record_fault(p, abort_flag, kRoleEpilogue, 0xff, w.tile);
+                *epi_ok = ok ? 1 : 0;
+            }
+            named_bar_sync(TC_EPI_BAR, TC_EPI_THREADS);
+            if (!*epi_ok) break;
+            mbar_wait(&tfull[b], use & 1u, abort_flag, p.timeout_ns, true);  // completed: no wait
+            tc_fence_after_sync();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+            const int gm = w.m_blk * 2 * TC_BM + (int)rank * TC_BM + row;
+#pragma unroll 1
+            for (int c = 0; c < w.width / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, r);
+                tmem_ld_wait();
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if (p.c_tma)
+                    store_chunk_tma(p, &tmC, warp_stage, stage_seq, lane, gm - lane,
+                                    w.n0 + c * 32, v);
+                else
+                    store_row_chunk(p, gm, w.n0 + c * 32, v);
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(b ? tempty_cl1 : tempty_cl0);
+        }
+    }
+
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores of C have landed
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // no remote arrive or pair MMA can still touch this CTA
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
@@ -484,6 +854,29 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer
 
 // Exactly one of st (library-owned workspace, grown on demand) and ext
 // (caller-provided scratch, never allocated) supplies the split-K storage.
+// Tensor map for TMA stores of C (rows of N elements, pitch ldc): boxes of
+// 32 x 32, swizzled as store_chunk_tma lays out its staging buffers.  Also
+// decides p.c_tma: TMA stores need a 16-byte aligned C with a pitch that is
+// a multiple of 16 bytes; otherwise the epilogue stores directly.
+bool make_c_map(CUtensorMap *map, TcParams &p) {
+    const int esz = p.c_f32 ? 4 : 2;
+    p.c_tma = ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) && ((p.ldc * esz) % 16 == 0);
+    if (!p.c_tma) {
+        memset(map, 0, sizeof(*map));
+        return true;
+    }
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.M};
+    cuuint64_t strides[1] = {(cuuint64_t)p.ldc * esz};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, p.c_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              p.C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              p.c_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN>
 int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *ext,
               TcParams &p, const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
@@ -496,11 +889,12 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
             return GEMM_ERR_CUDA;
         attr_done[device] = true;
     }
-    alignas(64) CUtensorMap ta, tb;
+    alignas(64) CUtensorMap ta, tb, tc;
     if (!make_map(&ta, A, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)lda, TC_BK, TC_BM))
         return GEMM_ERR_CUDA;
     if (!make_map(&tb, B, (uint64_t)p.N, (uint64_t)p.K, (uint64_t)ldb, 64, TC_BK))
         return GEMM_ERR_CUDA;
+    if (!make_c_map(&tc, p)) return GEMM_ERR_CUDA;
 
     p.num_m_blk = (p.M + TC_BM - 1) / TC_BM;
     p.num_n_blk = (p.N + BN - 1) / BN;
@@ -518,7 +912,42 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
     if (splits > p.num_kb) splits = p.num_kb;
     p.kb_per_split = (p.num_kb + splits - 1) / splits;
     p.splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;  // no empty slice
-    const long long units = tiles * p.splits;
+    if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    // Raster band: 8 M-blocks when A and B fit in L2 together (concurrent
+    // CTAs then share A and B blocks best); otherwise as many M-blocks as
+    // keep the band's A panel (128 rows x K bf16 each) within about 32 MiB
+    // of L2, so A is fetched from DRAM about once.  (Measured on GB300:
+    // 4096^3 is fastest with 8; 8192 x 14336 x 4096 with 32.)
+    {
+        const long long panel = (long long)TC_BM * p.K * 2;
+        const long long ab_bytes = 2ll * ((long long)p.M * p.K + (long long)p.K * p.N);
+        long long g = (ab_bytes <= (80ll << 20)) ? 8 : (32ll << 20) / (panel > 0 ? panel : 1);
+        if (g < 8) g = 8;
+        if (cfg.raster_group > 0) g = cfg.raster_group;
+        if (g > p.num_m_blk) g = p.num_m_blk;
+        p.group_m = (int)g;
+    }
+    // Wave quantisation: with P persistent CTAs, tiles beyond the last full
+    // wave are cut into 2 or 4 narrower sub-tiles when the partial wave
+    // leaves at least that many SMs per tile idle.
+    p.tiles_main = (int)tiles;
+    p.tail_split = 1;
+    if (p.splits == 1) {
+        const long long P = sm_count;
+        const long long rem = tiles % P;
+        long long f = rem ? P / rem : 1;
+        if (f > BN / 64) f = BN / 64;
+        if (f >= 4) f = 4;
+        else if (f >= 2) f = 2;
+        else f = 1;
+        if (cfg.tail_split_off) f = 1;
+        if (f > 1) {
+            p.tiles_main = (int)(tiles - rem);
+            p.tail_split = (int)f;
+        }
+    }
+    const long long units = (p.splits > 1) ? tiles * p.splits
+                                           : p.tiles_main + (tiles - p.tiles_main) * p.tail_split;
     if (units > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
     p.num_units = (int)units;
     p.ws = nullptr;
@@ -543,7 +972,102 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
         }
     }
     const int grid = (int)(units < sm_count ? units : sm_count);
-    bf16_tc_kernel<BN><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, p);
+    bf16_tc_kernel<BN><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, tc, p);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Largest number of CTA pairs that can be resident at once.  A pair must sit
+// in one GPC, so this can be below sm_count / 2.
+int max_resident_pairs(int device) {
+    static int cache[kMaxDevices] = {};
+    if (cache[device] > 0) return cache[device];
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2048, 1, 1);
+    lc.blockDim = dim3(TC_THREADS, 1, 1);
+    lc.dynamicSmemBytes = Tc2Cfg::SMEM_ALLOC;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, bf16_tc2_kernel, &lc) != cudaSuccess || n <= 0)
+        return 0;
+    cache[device] = n;
+    return n;
+}
+
+int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const uint16_t *B,
+               int64_t ldb, cudaStream_t stream) {
+    using Cfg = Tc2Cfg;
+    static bool attr_done[kMaxDevices] = {};
+    if (!attr_done[device]) {
+        if (cudaFuncSetAttribute(bf16_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_ALLOC) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        attr_done[device] = true;
+    }
+    const int pairs_max = max_resident_pairs(device);
+    if (pairs_max <= 0) return GEMM_ERR_CUDA;
+    alignas(64) CUtensorMap ta, tb, tc;
+    if (!make_map(&ta, A, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)lda, TC_BK, TC_BM))
+        return GEMM_ERR_CUDA;
+    if (!make_map(&tb, B, (uint64_t)p.N, (uint64_t)p.K, (uint64_t)ldb, 64, TC_BK))
+        return GEMM_ERR_CUDA;
+    if (!make_c_map(&tc, p)) return GEMM_ERR_CUDA;
+    const RuntimeConfig cfg = runtime_config();
+    p.num_m_blk = (p.M + 2 * TC_BM - 1) / (2 * TC_BM);  // 256-row pair tiles
+    p.num_n_blk = (p.N + Cfg::BN - 1) / Cfg::BN;
+    p.num_kb = (p.K + TC_BK - 1) / TC_BK;
+    p.splits = 1;
+    p.kb_per_split = p.num_kb;
+    p.ws = nullptr;
+    p.counters = nullptr;
+    const long long tiles = (long long)p.num_m_blk * p.num_n_blk;
+    if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    // Raster band in 256-row blocks: 1024 rows when A and B fit in L2
+    // together, else a band whose A panel takes about 32 MiB of L2.
+    {
+        const long long ab_bytes = 2ll * ((long long)p.M * p.K + (long long)p.K * p.N);
+        long long rows = (ab_bytes <= (80ll << 20)) ? 1024 : (32ll << 20) / ((long long)p.K * 2);
+        long long g = rows / (2 * TC_BM);
+        if (g < 4) g = 4;
+        if (cfg.raster_group > 0) g = cfg.raster_group;
+        if (g > p.num_m_blk) g = p.num_m_blk;
+        p.group_m = (int)g;
+    }
+    // Partial last wave: cut its tiles into two 128-column halves when that
+    // still leaves every half a pair of its own.
+    p.tiles_main = (int)tiles;
+    p.tail_split = 1;
+    {
+        const long long rem = tiles % pairs_max;
+        if (rem && !cfg.tail_split_off && pairs_max / rem >= 2) {
+            p.tiles_main = (int)(tiles - rem);
+            p.tail_split = 2;
+        }
+    }
+    const long long units = p.tiles_main + (tiles - p.tiles_main) * p.tail_split;
+    if (units > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    p.num_units = (int)units;
+    const int pairs = (int)(units < pairs_max ? units : pairs_max);
+
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(2 * pairs, 1, 1);
+    lc.blockDim = dim3(TC_THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_ALLOC;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, bf16_tc2_kernel, ta, tb, tc, p) != cudaSuccess)
+        return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -573,6 +1097,18 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
     if (p.fault_inject) consume_fault_inject();
     int bn = (int)cfg.bf16_tile_n;
     if (bn != 128 && bn != 256) bn = (N <= 128) ? 128 : 256;
+    // CTA pairs for problems with more than one 128-row block that give every
+    // SM whole tiles; the single-CTA kernel (with split-K) for small or
+    // short-and-deep problems.
+    bool pair = false;
+    if (cfg.cta_pair == 2) {
+        pair = true;
+    } else if (cfg.cta_pair == 0 && cfg.split_k == 0 && cfg.bf16_tile_n == 0 && M > TC_BM) {
+        const long long tiles1 = (long long)((M + TC_BM - 1) / TC_BM) * ((N + 255) / 256);
+        const int num_kb = (K + TC_BK - 1) / TC_BK;
+        pair = !(tiles1 * 2 <= sm_count && num_kb >= 8);
+    }
+    if (pair) return launch_tc2(device, p, A, lda, B, ldb, stream);
     return bn == 256 ? launch_tc<256>(device, sm_count, st, ext, p, A, lda, B, ldb, stream)
                      : launch_tc<128>(device, sm_count, st, ext, p, A, lda, B, ldb, stream);
 }

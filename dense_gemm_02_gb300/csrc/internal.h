@@ -49,6 +49,9 @@ struct RuntimeConfig {
     int64_t fault_inject;
     int64_t split_k;
     int64_t bf16_tile_n;
+    int64_t tail_split_off;
+    int64_t raster_group;
+    int64_t cta_pair;
 };
 RuntimeConfig runtime_config();
 void consume_fault_inject();
@@ -56,15 +59,16 @@ void consume_fault_inject();
 void set_last_kernel(const char *name);
 
 // Output-tile order shared by the kernels: tiles are walked in bands of
-// kRasterGroup M-blocks, N-blocks varying slowest within a band, so that
-// CTAs running at the same time reuse the same A rows and B columns in L2.
+// `group` M-blocks, N-blocks varying slowest within a band, so that CTAs
+// running at the same time reuse the same A rows and B columns in L2.
 constexpr int kRasterGroup = 8;
 __host__ __device__ __forceinline__ void grouped_tile_coords(int tile, int num_m, int num_n,
-                                                             int &m_blk, int &n_blk) {
-    const int per_group = kRasterGroup * num_n;
+                                                             int group_m, int &m_blk,
+                                                             int &n_blk) {
+    const int per_group = group_m * num_n;
     const int group = tile / per_group;
-    const int first_m = group * kRasterGroup;
-    const int gm = (num_m - first_m < kRasterGroup) ? num_m - first_m : kRasterGroup;
+    const int first_m = group * group_m;
+    const int gm = (num_m - first_m < group_m) ? num_m - first_m : group_m;
     const int r = tile - group * per_group;
     m_blk = first_m + r % gm;
     n_blk = r / gm;

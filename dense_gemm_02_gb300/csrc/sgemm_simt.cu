@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(THREADS, 2) sgemm_simt_kernel(const SimtParams
     const int b_off = wn * 64 + tn * 4;       // cols b_off..+3 and b_off+32..+35
 
     int m_blk, n_blk;
-    grouped_tile_coords(blockIdx.x, p.num_m_blk, p.num_n_blk, m_blk, n_blk);
+    grouped_tile_coords(blockIdx.x, p.num_m_blk, p.num_n_blk, kRasterGroup, m_blk, n_blk);
     const int m0 = m_blk * BM;
     const int n0 = n_blk * BN;
     const int KT = (p.K + BK - 1) / BK;

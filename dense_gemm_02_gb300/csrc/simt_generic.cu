@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(GTHREADS) gemm_simt_generic_kernel(const Gener
     __shared__ float As[GK][GB + 4];  // transposed: As[k][m]
     __shared__ float Bs[GK][GB + 4];
     int m_blk, n_blk;
-    grouped_tile_coords(blockIdx.x, num_m_blk, num_n_blk, m_blk, n_blk);
+    grouped_tile_coords(blockIdx.x, num_m_blk, num_n_blk, kRasterGroup, m_blk, n_blk);
     const int m0 = m_blk * GB, n0 = n_blk * GB;
     const int tid = threadIdx.x;
     const int tx = tid & 15, ty = tid >> 4;

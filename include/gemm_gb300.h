@@ -180,6 +180,12 @@ GEMM_API const char *gemm_status_string(int status);
  *                   its waits run out (tests the watchdog); resets itself
  *   "split_k"       0 auto, else the number of K slices for the tcgen05 kernel
  *   "bf16_tile_n"   0 auto, else 128 or 256 (tcgen05 tile width)
+ *   "tail_split_off" 1: do not cut the tiles of the last partial wave into
+ *                   narrower sub-tiles (tcgen05 kernel); 0 (default) cuts them
+ *   "raster_group"  0 auto, else the number of M-blocks (128 rows, or 256
+ *                   for CTA pairs) per raster band of the tcgen05 kernel
+ *   "cta_pair"      0 auto, 1 single-CTA tcgen05 kernel only, 2 always the
+ *                   CTA-pair (2-SM, cta_group::2) kernel
  * Returns GEMM_OK or GEMM_ERR_INVALID_ARG for an unknown key or value.
  */
 GEMM_API int gemm_set_config(const char *key, int64_t value);

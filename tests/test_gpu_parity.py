@@ -201,6 +201,67 @@ def test_bf16_tiles_and_split_k_integer(tile_n, split_k):
     assert C.guards_intact()
 
 
+# Tile counts that leave a partial last wave on a 152-SM part, so the tail
+# tiles are cut into 2 or 4 narrower sub-tiles; the ragged-N shape puts
+# sub-tiles wholly past the N edge.
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 256), (1792, 3328, 256), (1792, 3144, 200),
+                                   (1000, 2056, 72)])
+@pytest.mark.parametrize("tail_off", [0, 1])
+def test_bf16_partial_wave_tail_split_integer(M, N, K, tail_off):
+    seed = 555 + M + N + K
+    A = gi.draw("integer", seed, 0, (M, K), dtype="bf16")
+    B = gi.draw("integer", seed, 1, (K, N), dtype="bf16")
+    Cin = gi.draw("integer", seed, 2, (M, N), dtype="bf16")
+    g.set_config("tail_split_off", tail_off)
+    try:
+        C = run_bf16(A, B, Cin, 1.0, 1.0, "bf16")
+    finally:
+        g.set_config("tail_split_off", 0)
+    assert g.binding.last_kernel() == "bf16_tcgen05"
+    ref = oracle.round_bf16(oracle.gemm(A, B, Cin, alpha=1.0, beta=1.0))
+    got = C.result()
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} mismatches"
+    assert C.guards_intact()
+
+
+PAIR_SHAPES = [(1, 8, 8), (7, 72, 72), (129, 264, 1000), (257, 1000, 72), (300, 520, 776),
+               (1000, 1000, 1000), (2048, 2048, 512), (4096, 4096, 256), (1792, 3144, 200)]
+
+
+@pytest.mark.parametrize("cta_pair", [1, 2])
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+def test_bf16_single_and_pair_kernels_integer(M, N, K, cta_pair):
+    seed = 777 + M * 3 + N * 5 + K
+    A = gi.draw("integer", seed, 0, (M, K), dtype="bf16")
+    B = gi.draw("integer", seed, 1, (K, N), dtype="bf16")
+    Cin = gi.draw("integer", seed, 2, (M, N), dtype="bf16")
+    g.set_config("cta_pair", cta_pair)
+    try:
+        C = run_bf16(A, B, Cin, 0.5, 1.0, "bf16")
+    finally:
+        g.set_config("cta_pair", 0)
+    assert g.binding.last_kernel() == "bf16_tcgen05"
+    ref = oracle.round_bf16(oracle.gemm(A, B, Cin, alpha=0.5, beta=1.0))
+    got = C.result()
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} mismatches"
+    assert C.guards_intact()
+
+
+@pytest.mark.parametrize("out", ["bf16", "f32"])
+def test_bf16_pair_kernel_normal_tolerance(out):
+    M, N, K = 1000, 1288, 2056
+    A = gi.draw("normal", 4321, 0, (M, K), dtype="bf16")
+    B = gi.draw("normal", 4321, 1, (K, N), dtype="bf16")
+    g.set_config("cta_pair", 2)
+    try:
+        C = run_bf16(A, B, None, 1.0, 0.0, out)
+    finally:
+        g.set_config("cta_pair", 0)
+    ref = oracle.gemm(A, B)
+    assert bf16_tolerance_violations(widen(C.result(), out), ref) == 0
+    assert C.guards_intact()
+
+
 def test_bf16_forced_generic_matches_tcgen05_on_integers():
     M, N, K = 257, 384, 512
     A = gi.draw("integer", 31337, 0, (M, K), dtype="bf16")
