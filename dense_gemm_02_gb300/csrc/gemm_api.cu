@@ -152,6 +152,17 @@ extern "C" int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const floa
         e = launch_scale_c((int)M, (int)N, beta, C, ldc, true, s);
         set_last_kernel("scale_c");
     } else {
+        // TMA needs 16-byte aligned bases and pitches that are multiples of
+        // 16 bytes (4 floats); other operands take the cp.async kernel.
+        const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
+                            ((reinterpret_cast<uintptr_t>(B) & 15) == 0) && (lda % 4 == 0) &&
+                            (ldb % 4 == 0);
+        if (tma_ok && runtime_config().force_path != 1) {
+            rc = launch_sgemm_tma(st, (int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C,
+                                  ldc, s);
+            if (rc == GEMM_OK) set_last_kernel("sgemm_tma");
+            return rc;
+        }
         e = launch_sgemm_simt((int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C, ldc, s);
         set_last_kernel("sgemm_simt");
     }

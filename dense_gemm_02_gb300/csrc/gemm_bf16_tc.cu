@@ -107,6 +107,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
            ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same descriptor with its start address moved by `bytes` (a multiple of
+// 16).  Only the 14-bit start field changes; every address used here stays
+// below 228 KiB, so the field (address >> 4 < 16384) cannot carry.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
+    return desc + (bytes >> 4);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
 // A bf16 (7-9 = 1), B bf16 (10-12 = 1), A K-major (bit 15 = 0), B MN-major
 // (bit 16 = 1, B is row-major K x N), N >> 3 in bits 17-22, M >> 4 in 24-28.
@@ -415,8 +422,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
-            uint32_t it = 0, local = 0;
+            // A: K-major rows of 128 bytes, 8-row groups 1024 bytes apart; a
+            // K step of 16 moves 32 bytes along the row.  B: N-major; 64-column
+            // boxes B_BOX_BYTES apart, 8 K-rows 1024 bytes apart; a K step of 16
+            // is 16 rows (2048 bytes).  The loop below only adds offsets to
+            // these descriptors: a single issuing thread must spend as few
+            // instructions as possible between MMAs to keep the tensor pipe fed.
+            const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_addr(sB), Cfg::B_BOX_BYTES, 1024);
+            uint32_t s = 0, ph = 0, local = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
                 const Unit w = decode_unit<BN>(p, u);
@@ -431,29 +445,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
-                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1u;
+                uint32_t acc = 0;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(&full[s], ph, abort_flag, p.timeout_ns)) {
                         record_fault(p, abort_flag, kRoleMma, s, w.tile);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = a_base + s * Cfg::A_BYTES;
-                    const uint32_t sb = b_base + s * Cfg::B_BYTES;
-#pragma unroll
-                    for (int k = 0; k < TC_BK / TC_UMMA_K; ++k) {
-                        // A: K-major rows of 128 bytes, 8-row groups 1024 bytes
-                        // apart; a K step of 16 moves 32 bytes along the row.
-                        const uint64_t ad = smem_desc_sw128(sa + k * 32, 16, 1024);
-                        // B: N-major; 64-column boxes Cfg::B_BOX_BYTES apart,
-                        // 8 K-rows 1024 bytes apart; a K step of 16 is 16 rows.
-                        const uint64_t bd =
-                            smem_desc_sw128(sb + k * 16 * 128, Cfg::B_BOX_BYTES, 1024);
-                        umma_f16(d_tmem, ad, bd, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
-                    }
+                    const uint64_t ad = desc_add(a_desc0, s * Cfg::A_BYTES);
+                    const uint64_t bd = desc_add(b_desc0, s * Cfg::B_BYTES);
+                    umma_f16(d_tmem, ad, bd, idesc, acc);
+                    umma_f16(d_tmem, desc_add(ad, 32), desc_add(bd, 2048), idesc, 1u);
+                    umma_f16(d_tmem, desc_add(ad, 64), desc_add(bd, 4096), idesc, 1u);
+                    umma_f16(d_tmem, desc_add(ad, 96), desc_add(bd, 6144), idesc, 1u);
                     umma_commit(&empty[s]);  // frees the stage once these MMAs finish
+                    acc = 1u;
+                    if (++s == (uint32_t)S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 umma_commit(&tfull[b]);  // accumulator b is complete
@@ -720,8 +731,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && leader) {
-            const uint32_t a_base = smem_addr(sA), b_base = smem_addr(sB);
-            uint32_t it = 0, local = 0;
+            // Same descriptor scheme as the single-CTA kernel (offsets only).
+            const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), 16, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_addr(sB), Cfg::B_BOX_BYTES, 1024);
+            uint32_t s = 0, ph = 0, local = 0;
             bool ok = true;
             for (int u = pair; u < p.num_units && ok; u += npairs) {
                 const Unit w = decode_unit<BN>(p, u);
@@ -736,25 +749,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
-                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1u;
+                uint32_t acc = 0;
+                for (int kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!mbar_wait(&full[s], ph, abort_flag, p.timeout_ns)) {
                         record_fault(p, abort_flag, kRoleMma, s, w.tile);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t sa = a_base + s * Cfg::A_BYTES;
-                    const uint32_t sb = b_base + s * Cfg::B_BYTES;
-#pragma unroll
-                    for (int k = 0; k < TC_BK / TC_UMMA_K; ++k) {
-                        const uint64_t ad = smem_desc_sw128(sa + k * 32, 16, 1024);
-                        const uint64_t bd =
-                            smem_desc_sw128(sb + k * 16 * 128, Cfg::B_BOX_BYTES, 1024);
-                        umma_f16_pair(d_tmem, ad, bd, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
-                    }
+                    const uint64_t ad = desc_add(a_desc0, s * Cfg::A_BYTES);
+                    const uint64_t bd = desc_add(b_desc0, s * Cfg::B_BYTES);
+                    umma_f16_pair(d_tmem, ad, bd, idesc, acc);
+                    umma_f16_pair(d_tmem, desc_add(ad, 32), desc_add(bd, 2048), idesc, 1u);
+                    umma_f16_pair(d_tmem, desc_add(ad, 64), desc_add(bd, 4096), idesc, 1u);
+                    umma_f16_pair(d_tmem, desc_add(ad, 96), desc_add(bd, 6144), idesc, 1u);
                     umma_commit_pair(&empty[s], 0x3);  // frees stage s in both CTAs
+                    acc = 1u;
+                    if (++s == (uint32_t)S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 umma_commit_pair(&tfull[b], 0x3);  // accumulator b complete in both CTAs
@@ -1114,6 +1128,20 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
 }
 
 }  // namespace
+
+bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int launch_bf16_tcgen05(DeviceState *st, int M, int N, int K, float alpha, const uint16_t *A,
                         int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,

@@ -2,6 +2,7 @@
 // kernel translation units.  Nothing here is part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -15,7 +16,7 @@ constexpr int kMaxDevices = 64;
 // Device fault word layout (written once per fault by the first failing
 // thread with atomicCAS; 0 means no fault).
 constexpr unsigned long long kFaultFlag = 1ull << 63;
-enum FaultRole : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+enum FaultRole : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleSimt = 4 };
 
 __host__ __device__ constexpr unsigned long long fault_code(unsigned role, unsigned stage,
                                                             unsigned tile) {
@@ -74,11 +75,25 @@ __host__ __device__ __forceinline__ void grouped_tile_coords(int tile, int num_m
     n_blk = r / gm;
 }
 
+// Encodes a 2-D tiled tensor map (cuTensorMapEncodeTiled through the
+// runtime's driver entry point): `inner` contiguous elements per row,
+// `outer` rows, `pitch_bytes` between rows, boxes of box_inner x box_outer.
+// Out-of-range reads return zero.  False if the driver call failed.
+bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
 // ---- kernel launchers (return cudaSuccess or the launch error) ----
 
 cudaError_t launch_sgemm_simt(int M, int N, int K, float alpha, const float *A, int64_t lda,
                               const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
                               cudaStream_t stream);
+
+// FP32 SGEMM fed by TMA.  Needs 16-byte aligned A/B bases and lda, ldb
+// multiples of 4.  Returns a gemm_status_t.
+int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const float *A,
+                     int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
+                     cudaStream_t stream);
 
 // Generic SIMT GEMM for any alignment; a_bf16/b_bf16 select bf16 operands,
 // c_f32 selects an fp32 (else bf16) C.

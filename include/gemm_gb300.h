@@ -163,7 +163,7 @@ GEMM_API int gemm_get_device_status(void *stream);
 
 /*
  * Details of the last recorded device fault (0 if none): bits 0-7 the role
- * (1 producer, 2 MMA issuer, 3 epilogue), bits 8-15 the pipeline stage,
+ * (1 producer, 2 MMA issuer, 3 epilogue, 4 FP32 kernel), bits 8-15 the pipeline stage,
  * bits 16-47 the tile index.  Does not clear it.
  */
 GEMM_API int64_t gemm_get_device_fault_info(void);
@@ -174,7 +174,8 @@ GEMM_API const char *gemm_status_string(int status);
 /*
  * Tuning and debugging knobs (process-wide).  Keys:
  *   "watchdog_ms"   time limit of one pipeline wait on the GPU, ms (default 2000)
- *   "force_path"    0 auto, 1 force the generic (non-TMA) kernels,
+ *   "force_path"    0 auto, 1 force the non-TMA kernels (cp.async SGEMM,
+ *                   generic BF16 kernel),
  *                   2 force the tcgen05 kernel (fails on misaligned input)
  *   "fault_inject"  1: the next tcgen05 launch withholds one pipeline stage so
  *                   its waits run out (tests the watchdog); resets itself
@@ -193,7 +194,8 @@ GEMM_API int gemm_get_config(const char *key, int64_t *value);
 
 /*
  * Name of the kernel the last successful gemm_* call on this host thread
- * launched ("sgemm_simt", "bf16_tcgen05", "bf16_simt", "scale_c", "none").
+ * launched ("sgemm_tma", "sgemm_simt", "bf16_tcgen05", "bf16_simt", "scale_c",
+ * "none").
  */
 GEMM_API const char *gemm_last_kernel(void);
 

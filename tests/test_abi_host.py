@@ -104,7 +104,8 @@ def test_config_keys(lib):
         b.set_config("no_such_key", 1)
     with pytest.raises(b.GemmError):
         b.set_config("bf16_tile_n", 96)
-    assert b.last_kernel() in {"none", "sgemm_simt", "bf16_tcgen05", "bf16_simt", "scale_c"}
+    assert b.last_kernel() in {"none", "sgemm_simt", "sgemm_tma", "bf16_tcgen05", "bf16_simt",
+                                "scale_c"}
 
 
 def test_package_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -46,7 +46,7 @@ def run_workload(w, A, B, Cin):
         dA, dB = f32_to_dev(A), f32_to_dev(B)
         dC = f32_to_dev(Cin) if Cin is not None else torch.empty((w.M, w.N), device="cuda")
         g.sgemm(dA, dB, dC, alpha=w.alpha, beta=w.beta)
-        want = "sgemm_simt"
+        want = "sgemm_tma"
     else:
         dA, dB = bf16_to_dev(A), bf16_to_dev(B)
         if Cin is not None:

@@ -86,7 +86,9 @@ def test_f32_integer_bit_exact(M, N, K):
     B = gi.draw("integer", seed, 1, (K, N))
     Cin = gi.draw("integer", seed, 2, (M, N))
     C = run_f32(A, B, Cin, 1.0, -1.0)
-    assert g.binding.last_kernel() == "sgemm_simt"
+    # rows TMA can fetch (pitches multiples of 4 floats) take the TMA kernel
+    want = "sgemm_tma" if (K % 4 == 0 and N % 4 == 0) else "sgemm_simt"
+    assert g.binding.last_kernel() == want
     ref = oracle.round_f32(oracle.gemm(A, B, Cin, alpha=1.0, beta=-1.0))
     assert np.array_equal(C.result(), ref)
     assert C.guards_intact()
@@ -115,6 +117,21 @@ def test_f32_pitched_operands(lda_pad, ldb_pad, ldc_pad):
     C = run_f32(A, B, Cin, 2.0, 0.5, lda=K + lda_pad, ldb=N + ldb_pad, ldc=N + ldc_pad)
     ref = oracle.round_f32(oracle.gemm(A, B, Cin, alpha=2.0, beta=0.5))
     assert np.array_equal(C.result(), ref)
+    assert C.guards_intact()
+
+
+@pytest.mark.parametrize("force", [0, 1])
+def test_f32_tma_and_cp_async_kernels_agree_exactly(force):
+    M, N, K = 300, 520, 776
+    A = gi.draw("integer", 2024, 0, (M, K))
+    B = gi.draw("integer", 2024, 1, (K, N))
+    g.set_config("force_path", force)
+    try:
+        C = run_f32(A, B, None, 1.0, 0.0)
+    finally:
+        g.set_config("force_path", 0)
+    assert g.binding.last_kernel() == ("sgemm_simt" if force else "sgemm_tma")
+    assert np.array_equal(C.result(), oracle.round_f32(oracle.gemm(A, B)))
     assert C.guards_intact()
 
 
