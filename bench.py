@@ -288,10 +288,17 @@ def config_block(workloads, args):
 
 
 def kernel_source_hash(w):
-    fname = "sgemm_simt.cu" if w.dtype == "f32" else "gemm_bf16_tc.cu"
+    fname = "sgemm_tma.cu" if w.dtype == "f32" else "gemm_bf16_tc.cu"
     path = os.path.join(ROOT, "dense_gemm_02_gb300", "csrc", fname)
     with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def kernel_name(w):
+    """The kernel the library launches for this workload (as profiled)."""
+    if w.dtype == "f32":
+        return "sgemm_tma_kernel"
+    return "bf16_tc2_kernel" if w.M > 128 and w.M * w.N >= 2 * 152 * 128 * 256 else "bf16_tc_kernel"
 
 
 def recorded_traffic(w):
@@ -410,21 +417,21 @@ def run_ours(args, dist):
                   "frac": tflops / fp32_peak, "traffic": recorded_traffic(w),
                   "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
                                  f"x {sm_max:.0f} MHz (max SM clock)",
-                  "kernel": "sgemm_simt_kernel"}
+                  "kernel": kernel_name(w)}
         elif w.M * w.N * w.K / (w.min_bytes() / 2) < 300:  # intensity below the ridge: HBM
             peak_bw = peaks["hbm_gbs"]
             rl = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
                   "frac": gbs / peak_bw, "traffic": recorded_traffic(w),
                   "peak_source": f"{peak_src} hbm_gbs",
                   "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
-                  "kernel": "bf16_tc_kernel"}
+                  "kernel": kernel_name(w)}
         else:
             pk = peaks["bf16_tflops"]
             rl = {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s",
                   "frac": tflops / pk, "traffic": recorded_traffic(w),
                   "peak_source": f"{peak_src} bf16_tflops (burst)",
                   "frac_of_sustained": tflops / peaks.get("bf16_tflops_sustained", pk),
-                  "kernel": "bf16_tc_kernel"}
+                  "kernel": kernel_name(w)}
         kernels[w.name] = entry
         rooflines[w.name] = rl
     dominant = max(range(nk), key=lambda i: statistics.mean(per_kernel_ms[i]))
