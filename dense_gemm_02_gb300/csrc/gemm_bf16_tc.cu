@@ -326,6 +326,58 @@ __device__ __forceinline__ void store_chunk_tma(const TcParams &p, const CUtenso
     ++seq;
 }
 
+// Stores C[gm][gn..gn+3] = alpha * acc + beta * C (one 16-byte fp32 or
+// 8-byte bf16 store when C rows are 16-byte aligned and the four columns
+// are inside C).
+__device__ __forceinline__ void store_quad(const TcParams &p, int gm, int gn, float4 acc) {
+    if (gm >= p.M || gn >= p.N) return;
+    const float alpha = p.alpha, beta = p.beta;
+    const float a[4] = {acc.x, acc.y, acc.z, acc.w};
+    float o[4];
+    if (p.c_f32) {
+        float *crow = static_cast<float *>(p.C) + (long long)gm * p.ldc;
+        if (p.c_vec && gn + 4 <= p.N) {
+            float4 *dst = reinterpret_cast<float4 *>(crow + gn);
+            const float4 c = (beta != 0.f) ? *dst : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[j] = beta != 0.f ? fmaf(alpha, a[j], beta * cv[j]) : alpha * a[j];
+            *dst = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (gn + j < p.N)
+                    crow[gn + j] = beta != 0.f ? fmaf(alpha, a[j], beta * crow[gn + j]) : alpha * a[j];
+        }
+    } else {
+        uint16_t *crow = static_cast<uint16_t *>(p.C) + (long long)gm * p.ldc;
+        if (p.c_vec && gn + 4 <= p.N) {
+            uint2 *dst = reinterpret_cast<uint2 *>(crow + gn);
+            uint2 c = make_uint2(0u, 0u);
+            if (beta != 0.f) c = *dst;
+            const uint32_t cw[2] = {c.x, c.y};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t h = (j & 1) ? (cw[j >> 1] >> 16) : (cw[j >> 1] & 0xFFFFu);
+                o[j] = beta != 0.f ? fmaf(alpha, a[j], beta * bf16_bits_to_float(h)) : alpha * a[j];
+            }
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(o[0], o[1]);
+            __nv_bfloat162 p1 = __floats2bfloat162_rn(o[2], o[3]);
+            *dst = make_uint2(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (gn + j < p.N) {
+                    const float v = beta != 0.f ? fmaf(alpha, a[j], beta * bf16_bits_to_float(crow[gn + j]))
+                                                : alpha * a[j];
+                    __nv_bfloat16 hb = __float2bfloat16_rn(v);
+                    crow[gn + j] = *reinterpret_cast<uint16_t *>(&hb);
+                }
+            }
+        }
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -547,34 +599,72 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 named_bar_sync(TC_EPI_BAR, TC_EPI_THREADS);
                 if (*last_flag) {
-                    // Last slice of this tile: sum slices 0..S-1 in order.
+                    // Last slice of this tile: all epilogue threads sum the
+                    // slices, each element over slices 0..S-1 in order, with
+                    // coalesced 16-byte loads (four columns per element).
                     __threadfence();
-                    if (gm < p.M) {
-                        const float *base = p.ws + ((size_t)tile * p.splits * TC_BM + row) * BN;
+                    const int rows = min(TC_BM, p.M - w.m_blk * TC_BM);
+                    const int c4n = BN / 4;
+                    const float *base = p.ws + (size_t)tile * p.splits * TC_BM * BN;
+                    const size_t slice = (size_t)TC_BM * BN;
+                    // Four elements per thread per pass and up to four slices
+                    // per step keep 16 independent loads in flight.
+                    const int total = rows * c4n;
+                    const float4 *b4 = reinterpret_cast<const float4 *>(base);
+                    const size_t slice4 = slice / 4;
 #pragma unroll 1
-                        for (int c = 0; c < BN / 32; ++c) {
-                            float v[32];
-#pragma unroll 1
-                            for (int s = 0; s < p.splits; ++s) {
-                                const float4 *src = reinterpret_cast<const float4 *>(
-                                    base + (size_t)s * TC_BM * BN + c * 32);
+                    for (int e0 = et; e0 < total; e0 += 4 * TC_EPI_THREADS) {
+                        float4 v[4];
+                        int off[4];
+                        bool in[4];
 #pragma unroll
-                                for (int j = 0; j < 8; ++j) {
-                                    const float4 x = __ldcg(src + j);
-                                    if (s == 0) {
-                                        v[4 * j] = x.x;
-                                        v[4 * j + 1] = x.y;
-                                        v[4 * j + 2] = x.z;
-                                        v[4 * j + 3] = x.w;
-                                    } else {
-                                        v[4 * j] += x.x;
-                                        v[4 * j + 1] += x.y;
-                                        v[4 * j + 2] += x.z;
-                                        v[4 * j + 3] += x.w;
-                                    }
+                        for (int q = 0; q < 4; ++q) {
+                            const int e = e0 + q * TC_EPI_THREADS;
+                            in[q] = e < total;
+                            const int r = e / c4n, c4 = e - r * c4n;
+                            off[q] = r * (BN / 4) + c4;
+                            v[q] = in[q] ? __ldcg(b4 + off[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        int sl = 1;
+#pragma unroll 1
+                        for (; sl + 3 < p.splits; sl += 4) {
+                            float4 x[4][4];
+#pragma unroll
+                            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    x[t][q] = in[q] ? __ldcg(b4 + (sl + t) * slice4 + off[q])
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    v[q].x += x[t][q].x;
+                                    v[q].y += x[t][q].y;
+                                    v[q].z += x[t][q].z;
+                                    v[q].w += x[t][q].w;
                                 }
+                        }
+#pragma unroll 1
+                        for (; sl < p.splits; ++sl) {
+                            float4 x[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                x[q] = in[q] ? __ldcg(b4 + sl * slice4 + off[q])
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                v[q].x += x[q].x;
+                                v[q].y += x[q].y;
+                                v[q].z += x[q].z;
+                                v[q].w += x[q].w;
                             }
-                            store_row_chunk(p, gm, gn0 + c * 32, v);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (!in[q]) continue;
+                            const int r = off[q] / (BN / 4), c4 = off[q] - r * (BN / 4);
+                            store_quad(p, w.m_blk * TC_BM + r, gn0 + 4 * c4, v[q]);
                         }
                     }
                     if (et == 0) p.counters[tile] = 0u;  // ready for the next launch
@@ -1110,7 +1200,17 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
     p.fault_inject = cfg.fault_inject ? 1 : 0;
     if (p.fault_inject) consume_fault_inject();
     int bn = (int)cfg.bf16_tile_n;
-    if (bn != 128 && bn != 256) bn = (N <= 128) ? 128 : 256;
+    if (bn != 128 && bn != 256) {
+        bn = (N <= 128) ? 128 : 256;
+        // When 256-wide tiles are too few for the SMs (the split-K regime),
+        // 128-wide tiles need half as many K slices for the same parallelism:
+        // less partial-sum traffic and a shorter reduction (measured on the
+        // 64 x 8192 x 8192 shape: 42 us vs 52 us).
+        const long long tiles256 = (long long)((M + TC_BM - 1) / TC_BM) * ((N + 255) / 256);
+        if (bn == 256 && tiles256 * 2 <= sm_count && (K + TC_BK - 1) / TC_BK >= 8 &&
+            cfg.split_k == 0)
+            bn = 128;
+    }
     // CTA pairs for problems with more than one 128-row block that give every
     // SM whole tiles; the single-CTA kernel (with split-K) for small or
     // short-and-deep problems.
