@@ -234,8 +234,10 @@ def run_reference(args, dist):
 
     oracle.build()
     threads = oracle.default_threads()
-    # bounded sample: about a minute of oracle work over all steps
-    per_step_target = max(0.2, 60.0 / max(1, args.steps + args.warmup))
+    # bounded sample: about five times --cpu-seconds of oracle work over all
+    # steps (a minute by default), at least a few milliseconds per step
+    per_step_target = max(0.005, min(60.0, 5.0 * args.cpu_seconds) /
+                          max(1, args.steps + args.warmup))
     _flops, _dt, rows, _threads = oracle_sample_time(workloads, per_step_target)
     B_cache = {}
     inputs = [(w, *_sample_operands(w, rows, B_cache)) for w in workloads]
