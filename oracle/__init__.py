@@ -64,6 +64,8 @@ def _load():
         lib.oracle_round_f32.restype = None
         lib.oracle_widen_bf16.argtypes = [vp, vp, i64]
         lib.oracle_widen_bf16.restype = None
+        lib.oracle_epilogue.argtypes = [i64, i64, vp, i64, ci, vp, ci, dbl, ci, vp, i64]
+        lib.oracle_epilogue.restype = ci
         _lib = lib
         return lib
 
@@ -138,6 +140,46 @@ def gemm_entries(A, B, rows, cols, C=None, alpha=1.0, beta=0.0):
     if rc != 0:
         raise ValueError("oracle_gemm_entries rejected its arguments")
     return out
+
+
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+
+
+def _vector(x, name):
+    if x is None:
+        return F32, None, None
+    x = np.ascontiguousarray(x)
+    t = {np.dtype(np.float32): F32, np.dtype(np.uint16): BF16, np.dtype(np.float64): F64}.get(x.dtype)
+    if t is None:
+        raise TypeError(f"{name}: unsupported dtype {x.dtype}")
+    return t, x.ctypes.data, x
+
+
+def gemm_fused(A, B, C=None, alpha=1.0, beta=0.0, bias=None, act=ACT_NONE, threads=None,
+               M=None, N=None, K=None):
+    """act(alpha * A @ B + bias) + beta * C in double (A, B logical, row-major)."""
+    lib = _load()
+    R = gemm(A, B, None, alpha=alpha, beta=0.0, threads=threads, M=M, N=N, K=K)
+    tb, pb, _kb = _vector(bias, "bias")
+    if bias is not None and _kb.size != R.shape[1]:
+        raise ValueError("bias must hold N values")
+    tc, pc, ldc, _kc = _operand(C, "C")
+    rc = lib.oracle_epilogue(R.shape[0], R.shape[1], R.ctypes.data, max(1, R.shape[1]), tb, pb,
+                             int(act), float(beta), tc, pc, ldc)
+    if rc != 0:
+        raise ValueError("oracle_epilogue rejected its arguments")
+    return R
+
+
+def act_values(x, act) -> np.ndarray:
+    """The oracle's activation applied to double values (via its epilogue)."""
+    x = np.ascontiguousarray(x, dtype=np.float64).reshape(1, -1).copy()
+    lib = _load()
+    rc = lib.oracle_epilogue(1, x.shape[1], x.ctypes.data, x.shape[1], F32, None, int(act), 0.0,
+                             F32, None, 1)
+    if rc != 0:
+        raise ValueError("oracle_epilogue rejected its arguments")
+    return x.reshape(-1)
 
 
 def round_bf16(x) -> np.ndarray:

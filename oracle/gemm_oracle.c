@@ -200,3 +200,43 @@ void oracle_round_bf16(const double *x, uint16_t *out, int64_t n) {
 void oracle_widen_bf16(const uint16_t *x, double *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = load_elem(ORACLE_BF16, x, i);
 }
+
+/*
+ * Fused epilogue, applied to R = alpha * op(A) * op(B) computed by
+ * oracle_gemm with beta = 0:  R = act(R + bias) + beta * C.
+ *
+ * Follows the fused "normalise, GELU, residual add" kernel of the "Z-Turbo"
+ * tuning page (lanjinlin.com.cn), section 2.1: the activation is applied
+ * first and the residual (here beta * C) is added after it; and the
+ * epilogue customisations (GELU, residual) named by "Blackwell BF16 GEMM
+ * ..." (lshu.cn), section 3.3.  The GELU is that page's tanh form,
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), here in double with the
+ * exact constant sqrt(2/pi) (the page prints it as 0.79788456).
+ *   bias: NULL or N values (type bias_type: 0 fp32, 1 bf16, 2 double)
+ *   act:  0 none, 1 relu (max(x, 0)), 2 gelu (tanh form)
+ *   beta == 0: C is not read.
+ */
+static double act_apply(int act, double x) {
+    if (act == 1) return x > 0.0 ? x : 0.0;
+    if (act == 2) {
+        const double k = sqrt(2.0 / 3.14159265358979323846);
+        return 0.5 * x * (1.0 + tanh(k * (x + 0.044715 * x * x * x)));
+    }
+    return x;
+}
+
+int oracle_epilogue(int64_t M, int64_t N, double *R, int64_t ldr, int bias_type,
+                    const void *bias, int act, double beta, int c_type, const void *C,
+                    int64_t ldc) {
+    if (M < 0 || N < 0 || !R || act < 0 || act > 2) return -1;
+    if (beta != 0.0 && !C) return -1;
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double v = R[i * ldr + j];
+            if (bias) v += load_elem(bias_type, bias, j);
+            v = act_apply(act, v);
+            if (beta != 0.0) v += beta * load_elem(c_type, C, i * ldc + j);
+            R[i * ldr + j] = v;
+        }
+    return 0;
+}

@@ -285,3 +285,53 @@ def test_page_facts_fp16_is_not_bf16(oracle):
     # 65504 fits in bf16's range with room to spare, but is not exact in bf16
     b = oracle.round_bf16(np.array([facts["printed_max"]], dtype=np.float64))
     assert oracle.widen_bf16(b)[0] == 65536.0
+
+
+# ---------------------------------------------------------------- fused epilogue
+
+def test_gelu_tanh_constant_is_the_printed_one(oracle):
+    # "Z-Turbo" page, section 2.1 prints the constant as 0.79788456
+    assert abs(math.sqrt(2 / math.pi) - 0.79788456) < 5e-9
+
+
+def test_gelu_odd_part_identity_and_limits(oracle):
+    x = np.linspace(-8, 8, 2001)
+    g = oracle.act_values(x, oracle.ACT_GELU)
+    gm = oracle.act_values(-x, oracle.ACT_GELU)
+    # 0.5x(1+tanh(u)) - 0.5(-x)(1+tanh(-u)) = x for the tanh form
+    assert np.max(np.abs((g - gm) - x)) < 1e-12
+    assert oracle.act_values([0.0], oracle.ACT_GELU)[0] == 0.0
+    big = oracle.act_values([30.0, -30.0], oracle.ACT_GELU)
+    assert big[0] == 30.0 and abs(big[1]) < 1e-300 + 1e-12
+
+
+def test_gelu_tanh_close_to_erf_gelu(oracle):
+    # the tanh form approximates x * Phi(x) to a few 1e-4
+    x = np.linspace(-6, 6, 4001)
+    g = oracle.act_values(x, oracle.ACT_GELU)
+    exact = np.array([0.5 * v * (1 + math.erf(v / math.sqrt(2))) for v in x])
+    assert np.max(np.abs(g - exact)) < 5e-4
+
+
+def test_relu_and_none(oracle):
+    x = np.array([-2.5, -0.0, 0.0, 1e-300, 3.0])
+    assert oracle.act_values(x, oracle.ACT_RELU).tolist() == [0.0, 0.0, 0.0, 1e-300, 3.0]
+    assert np.array_equal(oracle.act_values(x, oracle.ACT_NONE), x)
+
+
+def test_fused_epilogue_order_bias_act_then_residual(oracle):
+    M, K, N = 6, 5, 7
+    A = gi.draw("integer", 91, 0, (M, K))
+    B = gi.draw("integer", 91, 1, (K, N))
+    C = gi.draw("integer", 91, 2, (M, N))
+    bias = gi.draw("integer", 91, 3, (1, N)).reshape(-1)
+    R = oracle.gemm_fused(A, B, C, alpha=0.5, beta=2.0, bias=bias, act=oracle.ACT_RELU)
+    lin = 0.5 * (A.astype(np.int64) @ B.astype(np.int64)) + bias.astype(np.float64)
+    expect = np.maximum(lin, 0.0) + 2.0 * C.astype(np.float64)
+    assert np.array_equal(R, expect)
+    # no bias, no activation: the plain GEMM
+    assert np.array_equal(oracle.gemm_fused(A, B, C, alpha=0.5, beta=2.0),
+                          oracle.gemm(A, B, C, alpha=0.5, beta=2.0))
+    # bf16 bias widens exactly
+    bb = gi.f32_to_bf16_bits(bias.astype(np.float32))
+    assert np.array_equal(oracle.gemm_fused(A, B, bias=bb), oracle.gemm_fused(A, B, bias=bias))
