@@ -2,14 +2,15 @@
 
 Two hand-written CUDA kernels behind a C ABI (include/gemm_gb300.h):
 an FP32 SGEMM on the CUDA cores and a BF16 x BF16 -> FP32-accumulate GEMM on
-the tcgen05 tensor cores.  This package is the thin Python binding.
+the tcgen05 tensor cores, both with transposed-operand layouts and a fused
+bias / activation epilogue.  This package is the thin Python binding.
 """
 
 from . import binding
-from .api import gemm, gemm_bf16, sgemm
+from .api import gemm, gemm_bf16, gemm_ex, sgemm
 from .binding import GemmError, get_config, set_config
 
-__all__ = ["gemm", "gemm_bf16", "sgemm", "binding", "GemmError", "get_config",
+__all__ = ["gemm", "gemm_bf16", "gemm_ex", "sgemm", "binding", "GemmError", "get_config",
            "set_config", "flops"]
 
 

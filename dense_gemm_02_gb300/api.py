@@ -2,6 +2,8 @@
 
 ``sgemm`` and ``gemm_bf16`` take CUDA tensors (row-major, unit column
 stride) and enqueue one library call on the current torch stream.
+``gemm_ex`` adds transposed operands (a ``X.t()`` view is read in place)
+and the fused bias / activation epilogue.
 ``gemm`` additionally accepts host (CPU) tensors: it copies them to the
 device, runs the same call and copies C back, which is the end-to-end path
 a caller holding host buffers uses.  Nothing here computes: shapes, strides
@@ -37,6 +39,84 @@ def _shapes(A, B, C):
     if C is not None and tuple(C.shape) != (M, N):
         raise ValueError(f"C must be {(M, N)}, got {tuple(C.shape)}")
     return M, N, K
+
+
+_ACTS = {"none": _b.GEMM_ACT_NONE, "relu": _b.GEMM_ACT_RELU, "gelu": _b.GEMM_ACT_GELU_TANH,
+         "gelu_tanh": _b.GEMM_ACT_GELU_TANH}
+
+
+def _layout(t: torch.Tensor, name: str):
+    """(trans, ld) of a 2-D operand as stored: row-major (unit column
+    stride), or the transposed view of a row-major matrix (unit row
+    stride), whose stored form has the two dimensions swapped."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D")
+    r, c = t.shape
+    if c <= 1 or t.stride(1) == 1:
+        return 0, (max(1, t.stride(0)) if r > 1 else max(1, c))
+    if r <= 1 or t.stride(0) == 1:
+        return 1, (max(1, t.stride(1)) if c > 1 else max(1, r))
+    raise ValueError(f"{name} must be row-major or the transpose of a row-major matrix")
+
+
+def gemm_ex(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
+            alpha: float = 1.0, beta: float = 0.0, bias: torch.Tensor | None = None,
+            act: str = "none", out_dtype=None, stream=None) -> torch.Tensor:
+    """C = act(alpha * A @ B + bias) + beta * C on CUDA tensors.
+
+    A (M x K) and B (K x N) may each be row-major or a transposed view of a
+    row-major matrix (``W.t()``); the library reads the stored layout
+    directly.  ``bias`` is None or a contiguous N-vector (float32 or
+    bfloat16); ``act`` is "none", "relu" or "gelu" (tanh form).  float32
+    A, B run the FP32 path (C float32); bfloat16 A, B the tensor cores (C
+    bfloat16 or float32)."""
+    if A.dtype != B.dtype or A.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("A and B must both be float32 or both bfloat16")
+    if not (A.is_cuda and B.is_cuda):
+        raise TypeError("A and B must be CUDA tensors")
+    if act not in _ACTS:
+        raise ValueError(f"act must be one of {sorted(_ACTS)}")
+    M, N, K = _shapes(A, B, C)
+    ta, lda = _layout(A, "A")
+    tb, ldb = _layout(B, "B")
+    bias_ptr, bias_type = None, _b.GEMM_OUT_F32
+    if bias is not None:
+        if bias.dim() != 1 or bias.numel() != N or not bias.is_cuda or not bias.is_contiguous():
+            raise ValueError(f"bias must be a contiguous CUDA vector of {N} values")
+        if bias.dtype == torch.float32:
+            bias_type = _b.GEMM_OUT_F32
+        elif bias.dtype == torch.bfloat16:
+            bias_type = _b.GEMM_OUT_BF16
+        else:
+            raise TypeError("bias must be float32 or bfloat16")
+        bias_ptr = bias.data_ptr()
+    opts = _b.make_opts(ta, tb, bias_ptr, bias_type, _ACTS[act])
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs an input C")
+        od = torch.float32 if A.dtype == torch.float32 else (out_dtype or torch.bfloat16)
+        C = torch.empty((M, N), dtype=od, device=A.device)
+    if not C.is_cuda:
+        raise TypeError("C must be a CUDA tensor")
+    if A.dtype == torch.float32:
+        if C.dtype != torch.float32:
+            raise TypeError("C must be float32 for float32 operands")
+        rc = _b.gemm_f32_ex(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                            float(beta), C.data_ptr(), _row_major(C, "C"), opts,
+                            _stream_handle(stream))
+        _b.check(rc, "gemm_f32_ex")
+        return C
+    if C.dtype == torch.bfloat16:
+        c_type = _b.GEMM_OUT_BF16
+    elif C.dtype == torch.float32:
+        c_type = _b.GEMM_OUT_F32
+    else:
+        raise TypeError("C must be bfloat16 or float32")
+    rc = _b.gemm_bf16_ex(M, N, K, float(alpha), A.data_ptr(), lda, B.data_ptr(), ldb,
+                         float(beta), C.data_ptr(), _row_major(C, "C"), c_type, opts,
+                         _stream_handle(stream))
+    _b.check(rc, "gemm_bf16_ex")
+    return C
 
 
 def sgemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,

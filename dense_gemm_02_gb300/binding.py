@@ -28,6 +28,18 @@ GEMM_ERR_SCRATCH_LIMIT = -9
 GEMM_OUT_BF16 = 0
 GEMM_OUT_F32 = 1
 
+GEMM_ACT_NONE = 0
+GEMM_ACT_RELU = 1
+GEMM_ACT_GELU_TANH = 2
+
+
+class GemmOpts(ctypes.Structure):
+    """gemm_opts_t: operand layouts and fused epilogue of the *_ex calls."""
+
+    _fields_ = [("trans_a", ctypes.c_int), ("trans_b", ctypes.c_int),
+                ("bias", ctypes.c_void_p), ("bias_type", ctypes.c_int),
+                ("act", ctypes.c_int)]
+
 # Every exported symbol of the C ABI, with (restype, argtypes).
 _i64, _f32, _vp, _int, _cp = (ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
                               ctypes.c_char_p)
@@ -37,6 +49,10 @@ SIGNATURES = {
                          _vp]),
     "gemm_bf16_noalloc": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                                  _int, _vp]),
+    "gemm_bf16_ex": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _int,
+                            ctypes.POINTER(GemmOpts), _vp]),
+    "gemm_f32_ex": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
+                           ctypes.POINTER(GemmOpts), _vp]),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_get_device_fault_info": (_i64, []),
     "gemm_status_string": (_cp, [_int]),
@@ -108,6 +124,24 @@ def gemm_bf16_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stre
     """Raw call of the allocation-free variant (split-K scratch in a static
     device array); same arguments as gemm_bf16."""
     return lib().gemm_bf16_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, stream)
+
+
+def make_opts(trans_a=False, trans_b=False, bias=None, bias_type=GEMM_OUT_F32,
+              act=GEMM_ACT_NONE) -> GemmOpts:
+    """A gemm_opts_t; bias is a device address (int) or None."""
+    return GemmOpts(int(bool(trans_a)), int(bool(trans_b)), bias, int(bias_type), int(act))
+
+
+def gemm_bf16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, opts, stream) -> int:
+    """Raw call of the extended BF16 GEMM; opts is a GemmOpts or None."""
+    ptr = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_bf16_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, ptr, stream)
+
+
+def gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, opts, stream) -> int:
+    """Raw call of the extended FP32 GEMM; opts is a GemmOpts or None."""
+    ptr = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ptr, stream)
 
 
 def get_device_status(stream=None) -> int:

@@ -48,11 +48,23 @@ size_t span_bytes(int64_t rows, int64_t cols, int64_t ld, size_t esz) {
 int validate_gemm_args(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                        size_t a_esz, const void *B, int64_t ldb, size_t b_esz, float beta,
                        const void *C, int64_t ldc, size_t c_esz) {
+    return validate_gemm_args_ex(M, N, K, alpha, A, lda, a_esz, false, B, ldb, b_esz, false, beta,
+                                 C, ldc, c_esz);
+}
+
+int validate_gemm_args_ex(int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+                          int64_t lda, size_t a_esz, bool trans_a, const void *B, int64_t ldb,
+                          size_t b_esz, bool trans_b, float beta, const void *C, int64_t ldc,
+                          size_t c_esz) {
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim || lda > kMaxDim || ldb > kMaxDim ||
         ldc > kMaxDim)
         return GEMM_ERR_TOO_LARGE;
-    if (lda < (K > 1 ? K : 1) || ldb < (N > 1 ? N : 1) || ldc < (N > 1 ? N : 1))
+    // Stored shapes: A is M x K (K x M when transposed), B is K x N (N x K).
+    const int64_t a_rows = trans_a ? K : M, a_cols = trans_a ? M : K;
+    const int64_t b_rows = trans_b ? N : K, b_cols = trans_b ? K : N;
+    if (lda < (a_cols > 1 ? a_cols : 1) || ldb < (b_cols > 1 ? b_cols : 1) ||
+        ldc < (N > 1 ? N : 1))
         return GEMM_ERR_BAD_LD;
     if (M == 0 || N == 0) return 1;
     if (!C) return GEMM_ERR_NULLPTR;
@@ -60,8 +72,8 @@ int validate_gemm_args(int64_t M, int64_t N, int64_t K, float alpha, const void 
     if (reads_ab) {
         if (!A || !B) return GEMM_ERR_NULLPTR;
         const size_t cb = span_bytes(M, N, ldc, c_esz);
-        if (ranges_overlap(C, cb, A, span_bytes(M, K, lda, a_esz)) ||
-            ranges_overlap(C, cb, B, span_bytes(K, N, ldb, b_esz)))
+        if (ranges_overlap(C, cb, A, span_bytes(a_rows, a_cols, lda, a_esz)) ||
+            ranges_overlap(C, cb, B, span_bytes(b_rows, b_cols, ldb, b_esz)))
             return GEMM_ERR_ALIAS;
     }
     (void)beta;
@@ -95,29 +107,39 @@ int device_state(DeviceState **out) {
     return GEMM_OK;
 }
 
-int ensure_splitk_workspace(DeviceState *st, size_t ws_bytes, size_t n_counters) {
+int stream_workspace(DeviceState *st, cudaStream_t stream, size_t ws_bytes, size_t n_counters,
+                     Workspace **out) {
     std::lock_guard<std::mutex> lock(g_state_mu);
-    if (st->splitk_ws_bytes < ws_bytes) {
-        // Stream-ordered work may still read the old buffer.
-        if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
-        if (st->splitk_ws) cudaFree(st->splitk_ws);
-        st->splitk_ws = nullptr;
-        st->splitk_ws_bytes = 0;
-        if (cudaMalloc(&st->splitk_ws, ws_bytes) != cudaSuccess) return GEMM_ERR_CUDA;
-        st->splitk_ws_bytes = ws_bytes;
+    Workspace *w = nullptr;
+    for (auto &p : st->workspaces)
+        if (p->stream == stream) w = p.get();
+    if (!w) {
+        st->workspaces.push_back(std::make_unique<Workspace>());
+        w = st->workspaces.back().get();
+        w->stream = stream;
     }
-    if (st->splitk_counters_n < n_counters) {
+    if (w->ws_bytes < ws_bytes) {
+        // Work already queued on this stream may still read the old buffer.
         if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
-        if (st->splitk_counters) cudaFree(st->splitk_counters);
-        st->splitk_counters = nullptr;
-        st->splitk_counters_n = 0;
-        if (cudaMalloc(&st->splitk_counters, n_counters * sizeof(unsigned)) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        if (cudaMemset(st->splitk_counters, 0, n_counters * sizeof(unsigned)) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
-        st->splitk_counters_n = n_counters;
+        if (w->ws) cudaFree(w->ws);
+        w->ws = nullptr;
+        w->ws_bytes = 0;
+        if (cudaMalloc(&w->ws, ws_bytes) != cudaSuccess) return GEMM_ERR_CUDA;
+        w->ws_bytes = ws_bytes;
     }
+    if (w->counters_n < n_counters) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+        if (w->counters) cudaFree(w->counters);
+        w->counters = nullptr;
+        w->counters_n = 0;
+        if (cudaMalloc(&w->counters, n_counters * sizeof(unsigned)) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaMemset(w->counters, 0, n_counters * sizeof(unsigned)) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+        w->counters_n = n_counters;
+    }
+    *out = w;
     return GEMM_OK;
 }
 
@@ -133,64 +155,120 @@ void set_last_kernel(const char *name) { t_last_kernel = name; }
 
 }  // namespace gemm
 
-using namespace gemm;
+namespace gemm {
+namespace {
 
-extern "C" int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
-                        int64_t lda, const float *B, int64_t ldb, float beta, float *C,
-                        int64_t ldc, void *stream) {
-    int rc = validate_gemm_args(M, N, K, alpha, A, lda, 4, B, ldb, 4, beta, C, ldc, 4);
+// Checks the public options and converts them.  A NULL opts gives the
+// plain layouts and epilogue.
+int convert_opts(const gemm_opts_t *opts, GemmOpts *out) {
+    *out = GemmOpts{0, 0, nullptr, 0, GEMM_ACT_NONE};
+    if (!opts) return GEMM_OK;
+    if ((opts->trans_a != 0 && opts->trans_a != 1) || (opts->trans_b != 0 && opts->trans_b != 1))
+        return GEMM_ERR_INVALID_ARG;
+    if (opts->act != GEMM_ACT_NONE && opts->act != GEMM_ACT_RELU &&
+        opts->act != GEMM_ACT_GELU_TANH)
+        return GEMM_ERR_INVALID_ARG;
+    if (opts->bias_type != GEMM_OUT_BF16 && opts->bias_type != GEMM_OUT_F32)
+        return GEMM_ERR_INVALID_ARG;
+    out->trans_a = opts->trans_a;
+    out->trans_b = opts->trans_b;
+    out->bias = opts->bias;
+    out->bias_f32 = (opts->bias_type == GEMM_OUT_F32) ? 1 : 0;
+    out->act = opts->act;
+    return GEMM_OK;
+}
+
+bool has_epilogue(const GemmOpts &o) { return o.bias != nullptr || o.act != GEMM_ACT_NONE; }
+
+// Shared by the plain and extended FP32 entry points.
+int run_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+            const float *B, int64_t ldb, float beta, float *C, int64_t ldc, const GemmOpts &o,
+            void *stream) {
+    int rc = validate_gemm_args_ex(M, N, K, alpha, A, lda, 4, o.trans_a, B, ldb, 4, o.trans_b,
+                                   beta, C, ldc, 4);
     if (rc == 1) {
         set_last_kernel("none");
         return GEMM_OK;
     }
     if (rc != GEMM_OK) return rc;
+    if (o.bias && ranges_overlap(C, span_bytes(M, N, ldc, 4), o.bias,
+                                 (size_t)N * (o.bias_f32 ? 4 : 2)))
+        return GEMM_ERR_ALIAS;
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != GEMM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool epi = has_epilogue(o);
     cudaError_t e;
     if (alpha == 0.f || K == 0) {
-        e = launch_scale_c((int)M, (int)N, beta, C, ldc, true, s);
-        set_last_kernel("scale_c");
-    } else {
-        // TMA needs 16-byte aligned bases and pitches that are multiples of
-        // 16 bytes (4 floats); other operands take the cp.async kernel.
-        const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
-                            ((reinterpret_cast<uintptr_t>(B) & 15) == 0) && (lda % 4 == 0) &&
-                            (ldb % 4 == 0);
-        if (tma_ok && runtime_config().force_path != 1) {
-            rc = launch_sgemm_tma(st, (int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C,
-                                  ldc, s);
-            if (rc == GEMM_OK) set_last_kernel("sgemm_tma");
-            return rc;
+        if (!epi) {
+            e = launch_scale_c((int)M, (int)N, beta, C, ldc, true, s);
+            set_last_kernel("scale_c");
+        } else {  // act(bias) + beta * C: the generic kernel with an empty K loop
+            e = launch_gemm_simt_generic((int)M, (int)N, 0, alpha, nullptr, 1, nullptr, 1, beta,
+                                         C, ldc, false, true, &o, s);
+            set_last_kernel("f32_simt");
         }
+        return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+    // TMA needs 16-byte aligned bases and pitches that are multiples of 16
+    // bytes (4 floats).  Row-major operands take the TMA kernel (or the
+    // cp.async kernel without an epilogue); transposed ones, and misaligned
+    // ones with an epilogue, the generic kernel.
+    const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
+                        ((reinterpret_cast<uintptr_t>(B) & 15) == 0) && (lda % 4 == 0) &&
+                        (ldb % 4 == 0);
+    const bool row_major = !o.trans_a && !o.trans_b;
+    if (row_major && tma_ok && runtime_config().force_path != 1) {
+        rc = launch_sgemm_tma(st, (int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C, ldc,
+                              &o, s);
+        if (rc == GEMM_OK) set_last_kernel("sgemm_tma");
+        return rc;
+    }
+    if (row_major && !epi) {
         e = launch_sgemm_simt((int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C, ldc, s);
         set_last_kernel("sgemm_simt");
+    } else {
+        e = launch_gemm_simt_generic((int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                     false, true, &o, s);
+        set_last_kernel("f32_simt");
     }
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-extern "C" int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
-                         int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,
-                         int64_t ldc, int c_type, void *stream) {
+// Shared by the plain and extended BF16 entry points.
+int run_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A, int64_t lda,
+             const uint16_t *B, int64_t ldb, float beta, void *C, int64_t ldc, int c_type,
+             const GemmOpts &o, void *stream) {
     if (c_type != GEMM_OUT_BF16 && c_type != GEMM_OUT_F32) return GEMM_ERR_INVALID_ARG;
     const bool c_f32 = (c_type == GEMM_OUT_F32);
-    int rc = validate_gemm_args(M, N, K, alpha, A, lda, 2, B, ldb, 2, beta, C, ldc, c_f32 ? 4 : 2);
+    const size_t c_esz = c_f32 ? 4 : 2;
+    int rc = validate_gemm_args_ex(M, N, K, alpha, A, lda, 2, o.trans_a, B, ldb, 2, o.trans_b,
+                                   beta, C, ldc, c_esz);
     if (rc == 1) {
         set_last_kernel("none");
         return GEMM_OK;
     }
     if (rc != GEMM_OK) return rc;
+    if (o.bias && ranges_overlap(C, span_bytes(M, N, ldc, c_esz), o.bias,
+                                 (size_t)N * (o.bias_f32 ? 4 : 2)))
+        return GEMM_ERR_ALIAS;
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != GEMM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (alpha == 0.f || K == 0) {
-        set_last_kernel("scale_c");
-        return launch_scale_c((int)M, (int)N, beta, C, ldc, c_f32, s) == cudaSuccess
-                   ? GEMM_OK
-                   : GEMM_ERR_CUDA;
+        cudaError_t e;
+        if (!has_epilogue(o)) {
+            e = launch_scale_c((int)M, (int)N, beta, C, ldc, c_f32, s);
+            set_last_kernel("scale_c");
+        } else {  // act(bias) + beta * C: the generic kernel with an empty K loop
+            e = launch_gemm_simt_generic((int)M, (int)N, 0, alpha, nullptr, 1, nullptr, 1, beta,
+                                         C, ldc, true, c_f32, &o, s);
+            set_last_kernel("bf16_simt");
+        }
+        return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
     // TMA needs 16-byte aligned bases and row pitches that are multiples of
-    // 16 bytes (8 bf16 elements).
+    // 16 bytes (8 bf16 elements), in either stored layout.
     const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
                         ((reinterpret_cast<uintptr_t>(B) & 15) == 0) && (lda % 8 == 0) &&
                         (ldb % 8 == 0);
@@ -198,14 +276,53 @@ extern "C" int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uin
     if (force == 2 && !tma_ok) return GEMM_ERR_INVALID_ARG;
     if (tma_ok && force != 1) {
         rc = launch_bf16_tcgen05(st, (int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C, ldc,
-                                 c_f32, s);
+                                 c_f32, &o, s);
         if (rc == GEMM_OK) set_last_kernel("bf16_tcgen05");
         return rc;
     }
     const cudaError_t e = launch_gemm_simt_generic((int)M, (int)N, (int)K, alpha, A, lda, B, ldb,
-                                                   beta, C, ldc, true, c_f32, s);
+                                                   beta, C, ldc, true, c_f32, &o, s);
     if (e == cudaSuccess) set_last_kernel("bf16_simt");
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gemm
+
+using namespace gemm;
+
+extern "C" int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                        int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                        int64_t ldc, void *stream) {
+    GemmOpts o;
+    convert_opts(nullptr, &o);
+    return run_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, o, stream);
+}
+
+extern "C" int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                           int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                           int64_t ldc, const gemm_opts_t *opts, void *stream) {
+    GemmOpts o;
+    const int rc = convert_opts(opts, &o);
+    if (rc != GEMM_OK) return rc;
+    return run_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, o, stream);
+}
+
+extern "C" int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                         int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,
+                         int64_t ldc, int c_type, void *stream) {
+    GemmOpts o;
+    convert_opts(nullptr, &o);
+    return run_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, o, stream);
+}
+
+extern "C" int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                            int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,
+                            int64_t ldc, int c_type, const gemm_opts_t *opts, void *stream) {
+    GemmOpts o;
+    const int rc = convert_opts(opts, &o);
+    if (rc != GEMM_OK) return rc;
+    return run_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, o, stream);
 }
 
 extern "C" int gemm_get_device_status(void *stream) {
@@ -223,10 +340,10 @@ extern "C" int gemm_get_device_status(void *stream) {
     // A kernel that gave up may have left split-K tile counters mid-count.
     {
         std::lock_guard<std::mutex> lock(g_state_mu);
-        if (st->splitk_counters &&
-            cudaMemset(st->splitk_counters, 0, st->splitk_counters_n * sizeof(unsigned)) !=
-                cudaSuccess)
-            return GEMM_ERR_CUDA;
+        for (auto &w : st->workspaces)
+            if (w->counters &&
+                cudaMemset(w->counters, 0, w->counters_n * sizeof(unsigned)) != cudaSuccess)
+                return GEMM_ERR_CUDA;
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
     return GEMM_ERR_DEVICE_TIMEOUT;
@@ -245,7 +362,7 @@ extern "C" const char *gemm_status_string(int status) {
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: a CUDA call failed";
         case GEMM_ERR_DEVICE_TIMEOUT:
             return "GEMM_ERR_DEVICE_TIMEOUT: a GPU pipeline wait ran out of time";
-        case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS: C overlaps A or B";
+        case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS: C overlaps A, B or the bias";
         case GEMM_ERR_TOO_LARGE: return "GEMM_ERR_TOO_LARGE: dimension exceeds 2^31-1";
         case GEMM_ERR_SCRATCH_LIMIT:
             return "GEMM_ERR_SCRATCH_LIMIT: needs more split-K scratch than the static maximum";
@@ -310,8 +427,10 @@ extern "C" int gemm_shutdown(void) {
     if (st.device < 0) return GEMM_OK;
     if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
     if (st.fault_word) cudaFree(st.fault_word);
-    if (st.splitk_ws) cudaFree(st.splitk_ws);
-    if (st.splitk_counters) cudaFree(st.splitk_counters);
+    for (auto &w : st.workspaces) {
+        if (w->ws) cudaFree(w->ws);
+        if (w->counters) cudaFree(w->counters);
+    }
     st = DeviceState{};
     return GEMM_OK;
 }

@@ -38,6 +38,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx_sm100.cuh"
 
@@ -94,6 +95,9 @@ struct TcParams {
     unsigned long long *fault_word;
     unsigned long long timeout_ns;
     int fault_inject;
+    EpiParams epi;  // bias / activation of the fused epilogue
+    int a_mn;       // A stored K x M (op(A) = A^T): MN-major A tiles
+    int b_kmaj;     // B stored N x K (op(B) = B^T): K-major B tiles
 };
 
 // Shared-memory matrix descriptor of tcgen05 (PTX ISA, "matrix descriptor"):
@@ -115,11 +119,34 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) {
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A bf16 (7-9 = 1), B bf16 (10-12 = 1), A K-major (bit 15 = 0), B MN-major
-// (bit 16 = 1, B is row-major K x N), N >> 3 in bits 17-22, M >> 4 in 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, int m = TC_BM) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(n >> 3) << 17) |
+// A bf16 (7-9 = 1), B bf16 (10-12 = 1), A major-ness in bit 15 (0: K-major,
+// A row-major M x K; 1: MN-major, A stored K x M), B major-ness in bit 16
+// (1: MN-major, B row-major K x N; 0: K-major, B stored N x K), N >> 3 in
+// bits 17-22, M >> 4 in 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int n, int m, int a_mn, int b_kmaj) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(a_mn ? 1 : 0) << 15) |
+           ((uint32_t)(b_kmaj ? 0 : 1) << 16) | ((uint32_t)(n >> 3) << 17) |
            ((uint32_t)(m >> 4) << 24);
+}
+
+// Shared-memory operand tiles of one 64-deep K block, per layout (all with
+// the 128-byte swizzle, rows of 128 bytes, 8-row groups 1024 bytes apart):
+//   K-major   (A row-major, or B stored N x K): one row per M (or N) index
+//             holding 64 K values; a K step of 16 moves 32 bytes along the
+//             row.  Loaded as 64-wide K boxes of 128 (A) or 64 (B) rows.
+//   MN-major  (A stored K x M, or B row-major): one row per K index holding
+//             64 M (or N) values, 64-column boxes 8 KiB apart; a K step of 16
+//             is 16 rows, 2048 bytes.
+// Descriptors: K-major LBO 16 (unused with swizzling), SBO 1024; MN-major
+// LBO = 8192 (the next 64 columns), SBO 1024.
+struct OperandLayout {
+    uint32_t lbo;   // leading-dimension byte offset of the descriptor
+    uint32_t step;  // descriptor start-address step per K = 16, in 16-byte units
+};
+__device__ __forceinline__ OperandLayout operand_layout(int mn_major) {
+    // K-major: TC_UMMA_K bf16 values along a row; MN-major: TC_UMMA_K rows.
+    return mn_major ? OperandLayout{8192u, (TC_UMMA_K * 128u) >> 4}
+                    : OperandLayout{16u, (TC_UMMA_K * 2u) >> 4};
 }
 
 // One unit of work: output rows m_blk*128.., columns n0..n0+width-1, K
@@ -168,11 +195,12 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
 }
 
 // Stores 32 consecutive outputs of row gm starting at column gn:
-// C = alpha * acc + beta * C, converted to C's type.
-__device__ __forceinline__ void store_row_chunk(const TcParams &p, int gm, int gn,
+// C = alpha * acc + beta * C, converted to C's type.  (With the fused
+// epilogue, acc already holds act(alpha * acc + bias) and alpha is 1.)
+__device__ __forceinline__ void store_row_chunk(const TcParams &p, float alpha, int gm, int gn,
                                                 const float (&acc)[32]) {
     if (gm >= p.M) return;
-    const float alpha = p.alpha, beta = p.beta;
+    const float beta = p.beta;
     if (p.c_f32) {
         float *crow = static_cast<float *>(p.C) + (long long)gm * p.ldc;
         if (p.c_vec && gn + 32 <= p.N) {
@@ -247,11 +275,12 @@ __device__ __forceinline__ void store_row_chunk(const TcParams &p, int gm, int g
 // at c ^ (row & 7); bf16 rows of 64 bytes with chunk c at c ^ ((row >> 1) & 3).
 // Stores are asynchronous; a buffer is reused once the store issued two
 // chunks earlier has finished reading it.
-__device__ __forceinline__ void store_chunk_tma(const TcParams &p, const CUtensorMap *tmC,
+__device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha,
+                                                const CUtensorMap *tmC,
                                                 uint8_t *warp_stage, uint32_t &seq, int lane,
                                                 int gm0, int gn, const float (&acc)[32]) {
     const int gm = gm0 + lane;
-    const float alpha = p.alpha, beta = p.beta;
+    const float beta = p.beta;
     float o[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) o[j] = alpha * acc[j];
@@ -329,9 +358,10 @@ __device__ __forceinline__ void store_chunk_tma(const TcParams &p, const CUtenso
 // Stores C[gm][gn..gn+3] = alpha * acc + beta * C (one 16-byte fp32 or
 // 8-byte bf16 store when C rows are 16-byte aligned and the four columns
 // are inside C).
-__device__ __forceinline__ void store_quad(const TcParams &p, int gm, int gn, float4 acc) {
+__device__ __forceinline__ void store_quad(const TcParams &p, float alpha, int gm, int gn,
+                                           float4 acc) {
     if (gm >= p.M || gn >= p.N) return;
-    const float alpha = p.alpha, beta = p.beta;
+    const float beta = p.beta;
     const float a[4] = {acc.x, acc.y, acc.z, acc.w};
     float o[4];
     if (p.c_f32) {
@@ -378,7 +408,78 @@ __device__ __forceinline__ void store_quad(const TcParams &p, int gm, int gn, fl
     }
 }
 
-template <int BN>
+
+// TMA producer of the single-CTA kernel (lane 0 of warp 0) for one operand
+// layout: A_MN, A stored K x M (two 64 (M) x 64 (K) boxes per stage); B_KM,
+// B stored N x K (64 (K) x 64 (N) boxes); else row-major A (one 64 (K) x
+// 128 (M) box) and B (64 (N) x 64 (K) boxes).  Every layout fills a stage
+// with the same bytes.
+template <int BN, bool A_MN, bool B_KM>
+__device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap *tmA,
+                                            const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
+                                            uint64_t *full, uint64_t *empty,
+                                            volatile int *abort_flag) {
+    using Cfg = TcCfg<BN>;
+    constexpr int S = Cfg::STAGES;
+    uint32_t it = 0;
+    int withheld = -1;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit<BN>(p, u);
+        if (w.n0 >= p.N) continue;  // sub-tile wholly past the N edge
+        const int boxes = w.width / 64;
+        const uint32_t tx = Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES;
+        const int m0 = w.m_blk * TC_BM;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) {
+                record_fault(p, abort_flag, kRoleProducer, s, w.tile);
+                ok = false;
+                break;
+            }
+            if (p.fault_inject && blockIdx.x == 0 && it == 0) {
+                withheld = 0;  // test hook: this stage is never filled
+                continue;
+            }
+            mbar_arrive_expect_tx(&full[s], tx);
+            uint8_t *a_dst = sA + s * Cfg::A_BYTES;
+            const int k0 = kb * TC_BK;
+            if constexpr (A_MN) {
+                tma_load_2d(a_dst, tmA, &full[s], m0, k0);
+                tma_load_2d(a_dst + 8192, tmA, &full[s], m0 + 64, k0);
+            } else {
+                tma_load_2d(a_dst, tmA, &full[s], k0, m0);
+            }
+            uint8_t *b_dst = sB + s * Cfg::B_BYTES;
+            for (int j = 0; j < boxes; ++j) {
+                if constexpr (B_KM)
+                    tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[s], k0, w.n0 + j * 64);
+                else
+                    tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[s], w.n0 + j * 64, k0);
+            }
+        }
+    }
+    // Let every copy started here land before the CTA can exit.
+    const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+    for (uint32_t i = first; i < it; ++i) {
+        if ((int)i == withheld) continue;
+        mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
+    }
+}
+
+// Fused epilogue, first part: v[j] = act(alpha * v[j] + bias[gn + j]) for
+// the 32 columns gn..gn+31 (columns past N use bias[N - 1]; they are never
+// stored).  The store helpers then add beta * C with alpha = 1.
+__device__ __forceinline__ void apply_pre(const TcParams &p, int gn, float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = epi_pre(p.epi, p.alpha, v[j], min(gn + j, p.N - 1));
+}
+
+// EPI: the fused bias / activation epilogue is compiled in (a separate
+// instantiation, so the plain kernel's epilogue code stays as small as it
+// can be: its size measurably affects the main loop's speed).
+template <int BN, bool EPI>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
@@ -435,59 +536,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            uint32_t it = 0;
-            int withheld = -1;
-            bool ok = true;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-                const Unit w = decode_unit<BN>(p, u);
-                if (w.n0 >= p.N) continue;  // sub-tile wholly past the N edge
-                const int boxes = w.width / 64;
-                const uint32_t tx = Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES;
-                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1u;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) {
-                        record_fault(p, abort_flag, kRoleProducer, s, w.tile);
-                        ok = false;
-                        break;
-                    }
-                    if (p.fault_inject && blockIdx.x == 0 && it == 0) {
-                        withheld = 0;  // test hook: this stage is never filled
-                        continue;
-                    }
-                    mbar_arrive_expect_tx(&full[s], tx);
-                    tma_load_2d(sA + s * Cfg::A_BYTES, &tmA, &full[s], kb * TC_BK,
-                                w.m_blk * TC_BM);
-                    for (int j = 0; j < boxes; ++j)
-                        tma_load_2d(sB + s * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES, &tmB, &full[s],
-                                    w.n0 + j * 64, kb * TC_BK);
-                }
-            }
-            // Let every copy started here land before the CTA can exit.
-            const uint32_t first = it > (uint32_t)S ? it - S : 0u;
-            for (uint32_t i = first; i < it; ++i) {
-                if ((int)i == withheld) continue;
-                mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
-            }
+            // One loop per operand layout, chosen once: per-stage layout
+            // branches in this single thread measurably slow the pipeline.
+            if (!p.a_mn && !p.b_kmaj)
+                tc_producer<BN, false, false>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
+            else if (!p.a_mn)
+                tc_producer<BN, false, true>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
+            else if (!p.b_kmaj)
+                tc_producer<BN, true, false>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
+            else
+                tc_producer<BN, true, true>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            // A: K-major rows of 128 bytes, 8-row groups 1024 bytes apart; a
-            // K step of 16 moves 32 bytes along the row.  B: N-major; 64-column
-            // boxes B_BOX_BYTES apart, 8 K-rows 1024 bytes apart; a K step of 16
-            // is 16 rows (2048 bytes).  The loop below only adds offsets to
-            // these descriptors: a single issuing thread must spend as few
-            // instructions as possible between MMAs to keep the tensor pipe fed.
-            const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), 16, 1024);
-            const uint64_t b_desc0 = smem_desc_sw128(smem_addr(sB), Cfg::B_BOX_BYTES, 1024);
+            // Operand tiles as described at operand_layout.  The loop below
+            // only adds offsets to these descriptors: a single issuing thread
+            // must spend as few instructions as possible between MMAs to keep
+            // the tensor pipe fed.
+            const OperandLayout la = operand_layout(p.a_mn), lb = operand_layout(!p.b_kmaj);
+            const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), la.lbo, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_addr(sB), lb.lbo, 1024);
+            const uint32_t a1 = la.step, a2 = 2 * la.step, a3 = 3 * la.step;
+            const uint32_t b1 = lb.step, b2 = 2 * lb.step, b3 = 3 * lb.step;
             uint32_t s = 0, ph = 0, local = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
                 const Unit w = decode_unit<BN>(p, u);
                 if (w.n0 >= p.N) continue;
-                const uint32_t idesc = idesc_bf16_f32(w.width);
+                const uint32_t idesc = idesc_bf16_f32(w.width, TC_BM, p.a_mn, p.b_kmaj);
                 const uint32_t b = local & 1u, use = local >> 1;
                 ++local;
                 if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
@@ -508,9 +586,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint64_t ad = desc_add(a_desc0, s * Cfg::A_BYTES);
                     const uint64_t bd = desc_add(b_desc0, s * Cfg::B_BYTES);
                     umma_f16(d_tmem, ad, bd, idesc, acc);
-                    umma_f16(d_tmem, desc_add(ad, 32), desc_add(bd, 2048), idesc, 1u);
-                    umma_f16(d_tmem, desc_add(ad, 64), desc_add(bd, 4096), idesc, 1u);
-                    umma_f16(d_tmem, desc_add(ad, 96), desc_add(bd, 6144), idesc, 1u);
+                    umma_f16(d_tmem, ad + a1, bd + b1, idesc, 1u);
+                    umma_f16(d_tmem, ad + a2, bd + b2, idesc, 1u);
+                    umma_f16(d_tmem, ad + a3, bd + b3, idesc, 1u);
                     umma_commit(&empty[s]);  // frees the stage once these MMAs finish
                     acc = 1u;
                     if (++s == (uint32_t)S) {
@@ -563,11 +641,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if constexpr (EPI) apply_pre(p, gn0 + c * 32, v);
+                    const float alpha = EPI ? 1.f : p.alpha;
                     if (p.c_tma)
-                        store_chunk_tma(p, &tmC, warp_stage, stage_seq, lane, gm - lane,
+                        store_chunk_tma(p, alpha, &tmC, warp_stage, stage_seq, lane, gm - lane,
                                         gn0 + c * 32, v);
                     else
-                        store_row_chunk(p, gm, gn0 + c * 32, v);
+                        store_row_chunk(p, alpha, gm, gn0 + c * 32, v);
                 }
                 tc_fence_before_sync();
                 mbar_arrive(&tempty[b]);
@@ -664,7 +744,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         for (int q = 0; q < 4; ++q) {
                             if (!in[q]) continue;
                             const int r = off[q] / (BN / 4), c4 = off[q] - r * (BN / 4);
-                            store_quad(p, w.m_blk * TC_BM + r, gn0 + 4 * c4, v[q]);
+                            float4 x = v[q];
+                            if constexpr (EPI) {
+                                const int n = gn0 + 4 * c4, nl = p.N - 1;
+                                x.x = epi_pre(p.epi, p.alpha, x.x, min(n, nl));
+                                x.y = epi_pre(p.epi, p.alpha, x.y, min(n + 1, nl));
+                                x.z = epi_pre(p.epi, p.alpha, x.z, min(n + 2, nl));
+                                x.w = epi_pre(p.epi, p.alpha, x.w, min(n + 3, nl));
+                            }
+                            store_quad(p, EPI ? 1.f : p.alpha, w.m_blk * TC_BM + r, gn0 + 4 * c4,
+                                       x);
                         }
                     }
                     if (et == 0) p.counters[tile] = 0u;  // ready for the next launch
@@ -717,6 +806,75 @@ struct Tc2Cfg {
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
+// TMA producer of the CTA-pair kernel (lane 0 of warp 0 in both CTAs), for
+// one operand layout (as tc_producer).  Each CTA loads its own 128 rows of A
+// and its half of the tile's B columns; all copies complete on the even
+// CTA's full barrier.
+template <bool A_MN, bool B_KM>
+__device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMap *tmA,
+                                             const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
+                                             uint64_t *full, uint64_t *empty,
+                                             volatile int *abort_flag, uint32_t rank, int pair,
+                                             int npairs) {
+    using Cfg = Tc2Cfg;
+    constexpr int S = Cfg::STAGES;
+    const bool leader = (rank == 0);
+    uint32_t it = 0;
+    int withheld = -1;
+    bool ok = true;
+    for (int u = pair; u < p.num_units && ok; u += npairs) {
+        const Unit w = decode_unit<Cfg::BN>(p, u);
+        if (w.n0 >= p.N) continue;
+        const int half = w.width / 2;  // this CTA's B columns
+        const int boxes = half / 64;
+        const uint32_t tx = 2u * (Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES);
+        const int row0 = w.m_blk * 2 * TC_BM + (int)rank * TC_BM;
+        const int col0 = w.n0 + (int)rank * half;
+        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1u;
+            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) {
+                record_fault(p, abort_flag, kRoleProducer, s, w.tile);
+                ok = false;
+                break;
+            }
+            if (p.fault_inject && pair == 0 && leader && it == 0) {
+                withheld = 0;  // test hook: the stage's barrier never completes
+                continue;
+            }
+            const uint32_t full_cl = mapa_shared(smem_addr(&full[s]), 0);
+            if (leader) mbar_arrive_expect_tx(&full[s], tx);
+            uint8_t *a_dst = sA + s * Cfg::A_BYTES;
+            const int k0 = kb * TC_BK;
+            if constexpr (A_MN) {
+                tma_load_2d_pair(a_dst, tmA, full_cl, row0, k0);
+                tma_load_2d_pair(a_dst + 8192, tmA, full_cl, row0 + 64, k0);
+            } else {
+                tma_load_2d_pair(a_dst, tmA, full_cl, k0, row0);
+            }
+            uint8_t *b_dst = sB + s * Cfg::B_BYTES;
+            for (int j = 0; j < boxes; ++j) {
+                if constexpr (B_KM)
+                    tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, tmB, full_cl, k0,
+                                     col0 + j * 64);
+                else
+                    tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, tmB, full_cl,
+                                     col0 + j * 64, k0);
+            }
+        }
+    }
+    // The even CTA's full barriers count both CTAs' copies: wait for the
+    // ones still in flight before the pair may exit.
+    if (leader) {
+        const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+        for (uint32_t i = first; i < it; ++i) {
+            if ((int)i == withheld) continue;
+            mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
+        }
+    }
+}
+
+template <bool EPI>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     bf16_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -776,60 +934,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            uint32_t it = 0;
-            int withheld = -1;
-            bool ok = true;
-            for (int u = pair; u < p.num_units && ok; u += npairs) {
-                const Unit w = decode_unit<BN>(p, u);
-                if (w.n0 >= p.N) continue;
-                const int half = w.width / 2;         // this CTA's B columns
-                const int boxes = half / 64;
-                const uint32_t tx = 2u * (Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES);
-                const int row0 = w.m_blk * 2 * TC_BM + (int)rank * TC_BM;
-                const int col0 = w.n0 + (int)rank * half;
-                for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-                    const int s = it % S;
-                    const uint32_t ph = (it / S) & 1u;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) {
-                        record_fault(p, abort_flag, kRoleProducer, s, w.tile);
-                        ok = false;
-                        break;
-                    }
-                    if (p.fault_inject && pair == 0 && leader && it == 0) {
-                        withheld = 0;  // test hook: the stage's barrier never completes
-                        continue;
-                    }
-                    const uint32_t full_cl = mapa_shared(smem_addr(&full[s]), 0);
-                    if (leader) mbar_arrive_expect_tx(&full[s], tx);
-                    tma_load_2d_pair(sA + s * Cfg::A_BYTES, &tmA, full_cl, kb * TC_BK, row0);
-                    for (int j = 0; j < boxes; ++j)
-                        tma_load_2d_pair(sB + s * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES, &tmB,
-                                         full_cl, col0 + j * 64, kb * TC_BK);
-                }
-            }
-            // The even CTA's full barriers count both CTAs' copies: wait for
-            // the ones still in flight before the pair may exit.
-            if (leader) {
-                const uint32_t first = it > (uint32_t)S ? it - S : 0u;
-                for (uint32_t i = first; i < it; ++i) {
-                    if ((int)i == withheld) continue;
-                    mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
-                }
-            }
+            if (!p.a_mn && !p.b_kmaj)
+                tc2_producer<false, false>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank,
+                                           pair, npairs);
+            else if (!p.a_mn)
+                tc2_producer<false, true>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank,
+                                          pair, npairs);
+            else if (!p.b_kmaj)
+                tc2_producer<true, false>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank,
+                                          pair, npairs);
+            else
+                tc2_producer<true, true>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank,
+                                         pair, npairs);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && leader) {
             // Same descriptor scheme as the single-CTA kernel (offsets only).
-            const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), 16, 1024);
-            const uint64_t b_desc0 = smem_desc_sw128(smem_addr(sB), Cfg::B_BOX_BYTES, 1024);
+            const OperandLayout la = operand_layout(p.a_mn), lb = operand_layout(!p.b_kmaj);
+            const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), la.lbo, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_addr(sB), lb.lbo, 1024);
+            const uint32_t a1 = la.step, a2 = 2 * la.step, a3 = 3 * la.step;
+            const uint32_t b1 = lb.step, b2 = 2 * lb.step, b3 = 3 * lb.step;
             uint32_t s = 0, ph = 0, local = 0;
             bool ok = true;
             for (int u = pair; u < p.num_units && ok; u += npairs) {
                 const Unit w = decode_unit<BN>(p, u);
                 if (w.n0 >= p.N) continue;
-                const uint32_t idesc = idesc_bf16_f32(w.width, 2 * TC_BM);
+                const uint32_t idesc = idesc_bf16_f32(w.width, 2 * TC_BM, p.a_mn, p.b_kmaj);
                 const uint32_t b = local & 1u, use = local >> 1;
                 ++local;
                 if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
@@ -850,9 +983,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const uint64_t ad = desc_add(a_desc0, s * Cfg::A_BYTES);
                     const uint64_t bd = desc_add(b_desc0, s * Cfg::B_BYTES);
                     umma_f16_pair(d_tmem, ad, bd, idesc, acc);
-                    umma_f16_pair(d_tmem, desc_add(ad, 32), desc_add(bd, 2048), idesc, 1u);
-                    umma_f16_pair(d_tmem, desc_add(ad, 64), desc_add(bd, 4096), idesc, 1u);
-                    umma_f16_pair(d_tmem, desc_add(ad, 96), desc_add(bd, 6144), idesc, 1u);
+                    umma_f16_pair(d_tmem, ad + a1, bd + b1, idesc, 1u);
+                    umma_f16_pair(d_tmem, ad + a2, bd + b2, idesc, 1u);
+                    umma_f16_pair(d_tmem, ad + a3, bd + b3, idesc, 1u);
                     umma_commit_pair(&empty[s], 0x3);  // frees stage s in both CTAs
                     acc = 1u;
                     if (++s == (uint32_t)S) {
@@ -901,11 +1034,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if constexpr (EPI) apply_pre(p, w.n0 + c * 32, v);
+                const float alpha = EPI ? 1.f : p.alpha;
                 if (p.c_tma)
-                    store_chunk_tma(p, &tmC, warp_stage, stage_seq, lane, gm - lane,
+                    store_chunk_tma(p, alpha, &tmC, warp_stage, stage_seq, lane, gm - lane,
                                     w.n0 + c * 32, v);
                 else
-                    store_row_chunk(p, gm, w.n0 + c * 32, v);
+                    store_row_chunk(p, alpha, gm, w.n0 + c * 32, v);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -956,6 +1091,21 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of the A and B operands in the layouts p.a_mn / p.b_kmaj
+// select (see operand_layout): row-major A as 64 (K) x 128 (M) boxes,
+// A stored K x M as 64 (M) x 64 (K) boxes; row-major B as 64 (N) x 64 (K)
+// boxes, B stored N x K as 64 (K) x 64 (N) boxes.  Every box's x coordinate
+// is a multiple of 64 elements (128 bytes).
+bool make_ab_maps(CUtensorMap *ta, CUtensorMap *tb, const TcParams &p, const uint16_t *A,
+                  int64_t lda, const uint16_t *B, int64_t ldb) {
+    const uint64_t M = (uint64_t)p.M, N = (uint64_t)p.N, K = (uint64_t)p.K;
+    const bool ok_a = p.a_mn ? make_map(ta, A, M, K, (uint64_t)lda, 64, TC_BK)
+                             : make_map(ta, A, K, M, (uint64_t)lda, TC_BK, TC_BM);
+    const bool ok_b = p.b_kmaj ? make_map(tb, B, K, N, (uint64_t)ldb, TC_BK, 64)
+                               : make_map(tb, B, N, K, (uint64_t)ldb, 64, TC_BK);
+    return ok_a && ok_b;
+}
+
 // Exactly one of st (library-owned workspace, grown on demand) and ext
 // (caller-provided scratch, never allocated) supplies the split-K storage.
 // Tensor map for TMA stores of C (rows of N elements, pitch ldc): boxes of
@@ -988,16 +1138,17 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
     using Cfg = TcCfg<BN>;
     static bool attr_done[kMaxDevices] = {};
     if (!attr_done[device]) {
-        if (cudaFuncSetAttribute(bf16_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(bf16_tc_kernel<BN, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_ALLOC) != cudaSuccess ||
+            cudaFuncSetAttribute(bf16_tc_kernel<BN, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_ALLOC) != cudaSuccess)
             return GEMM_ERR_CUDA;
         attr_done[device] = true;
     }
     alignas(64) CUtensorMap ta, tb, tc;
-    if (!make_map(&ta, A, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)lda, TC_BK, TC_BM))
-        return GEMM_ERR_CUDA;
-    if (!make_map(&tb, B, (uint64_t)p.N, (uint64_t)p.K, (uint64_t)ldb, 64, TC_BK))
-        return GEMM_ERR_CUDA;
+    if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb)) return GEMM_ERR_CUDA;
     if (!make_c_map(&tc, p)) return GEMM_ERR_CUDA;
 
     p.num_m_blk = (p.M + TC_BM - 1) / TC_BM;
@@ -1069,14 +1220,18 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
             p.ws = ext->ws;
             p.counters = ext->counters;
         } else {
-            const int rc = ensure_splitk_workspace(st, ws_bytes, (size_t)tiles);
+            Workspace *w = nullptr;
+            const int rc = stream_workspace(st, stream, ws_bytes, (size_t)tiles, &w);
             if (rc != GEMM_OK) return rc;
-            p.ws = st->splitk_ws;
-            p.counters = st->splitk_counters;
+            p.ws = w->ws;
+            p.counters = w->counters;
         }
     }
     const int grid = (int)(units < sm_count ? units : sm_count);
-    bf16_tc_kernel<BN><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, tc, p);
+    if (p.epi.on)
+        bf16_tc_kernel<BN, true><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, tc, p);
+    else
+        bf16_tc_kernel<BN, false><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, tc, p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -1097,7 +1252,7 @@ int max_resident_pairs(int device) {
     lc.attrs = attr;
     lc.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, bf16_tc2_kernel, &lc) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, bf16_tc2_kernel<false>, &lc) != cudaSuccess || n <= 0)
         return 0;
     cache[device] = n;
     return n;
@@ -1108,7 +1263,11 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     using Cfg = Tc2Cfg;
     static bool attr_done[kMaxDevices] = {};
     if (!attr_done[device]) {
-        if (cudaFuncSetAttribute(bf16_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(bf16_tc2_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_ALLOC) != cudaSuccess ||
+            cudaFuncSetAttribute(bf16_tc2_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_ALLOC) != cudaSuccess)
             return GEMM_ERR_CUDA;
         attr_done[device] = true;
@@ -1116,10 +1275,7 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     const int pairs_max = max_resident_pairs(device);
     if (pairs_max <= 0) return GEMM_ERR_CUDA;
     alignas(64) CUtensorMap ta, tb, tc;
-    if (!make_map(&ta, A, (uint64_t)p.K, (uint64_t)p.M, (uint64_t)lda, TC_BK, TC_BM))
-        return GEMM_ERR_CUDA;
-    if (!make_map(&tb, B, (uint64_t)p.N, (uint64_t)p.K, (uint64_t)ldb, 64, TC_BK))
-        return GEMM_ERR_CUDA;
+    if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb)) return GEMM_ERR_CUDA;
     if (!make_c_map(&tc, p)) return GEMM_ERR_CUDA;
     const RuntimeConfig cfg = runtime_config();
     p.num_m_blk = (p.M + 2 * TC_BM - 1) / (2 * TC_BM);  // 256-row pair tiles
@@ -1170,8 +1326,9 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&lc, bf16_tc2_kernel, ta, tb, tc, p) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+    const cudaError_t e = p.epi.on ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true>, ta, tb, tc, p)
+                                   : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false>, ta, tb, tc, p);
+    if (e != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -1182,8 +1339,16 @@ namespace {
 int launch_common(int device, int sm_count, DeviceState *st, const ExternalScratch *ext,
                   unsigned long long *fault_word, int M, int N, int K, float alpha,
                   const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, float beta,
-                  void *C, int64_t ldc, bool c_f32, cudaStream_t stream) {
+                  void *C, int64_t ldc, bool c_f32, const GemmOpts *opts, cudaStream_t stream) {
     TcParams p{};
+    if (opts) {
+        p.a_mn = opts->trans_a ? 1 : 0;
+        p.b_kmaj = opts->trans_b ? 1 : 0;
+        p.epi.bias = opts->bias;
+        p.epi.bias_f32 = opts->bias_f32 ? 1 : 0;
+        p.epi.act = opts->act;
+        p.epi.on = (opts->bias != nullptr || opts->act != 0) ? 1 : 0;
+    }
     p.M = M;
     p.N = N;
     p.K = K;
@@ -1245,17 +1410,18 @@ bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
 
 int launch_bf16_tcgen05(DeviceState *st, int M, int N, int K, float alpha, const uint16_t *A,
                         int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,
-                        int64_t ldc, bool c_f32, cudaStream_t stream) {
+                        int64_t ldc, bool c_f32, const GemmOpts *opts, cudaStream_t stream) {
     return launch_common(st->device, st->sm_count, st, nullptr, st->fault_word, M, N, K, alpha,
-                         A, lda, B, ldb, beta, C, ldc, c_f32, stream);
+                         A, lda, B, ldb, beta, C, ldc, c_f32, opts, stream);
 }
 
 int launch_bf16_tcgen05_external(int device, int sm_count, const ExternalScratch &ext, int M,
                                  int N, int K, float alpha, const uint16_t *A, int64_t lda,
                                  const uint16_t *B, int64_t ldb, float beta, void *C,
-                                 int64_t ldc, bool c_f32, cudaStream_t stream) {
+                                 int64_t ldc, bool c_f32, const GemmOpts *opts,
+                                 cudaStream_t stream) {
     return launch_common(device, sm_count, nullptr, &ext, ext.fault_word, M, N, K, alpha, A, lda,
-                         B, ldb, beta, C, ldc, c_f32, stream);
+                         B, ldb, beta, C, ldc, c_f32, opts, stream);
 }
 
 }  // namespace gemm

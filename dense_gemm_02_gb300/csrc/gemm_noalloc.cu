@@ -104,5 +104,5 @@ extern "C" int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
     if (cudaMemsetAsync(ext.fault_word, 0, sizeof(unsigned long long), s) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return launch_bf16_tcgen05_external(device, slot->sm_count, ext, (int)M, (int)N, (int)K,
-                                        alpha, A, lda, B, ldb, beta, C, ldc, c_f32, s);
+                                        alpha, A, lda, B, ldb, beta, C, ldc, c_f32, nullptr, s);
 }

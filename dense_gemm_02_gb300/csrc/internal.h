@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <memory>
+#include <vector>
 
 #include "gemm_gb300.h"
 
@@ -25,24 +27,35 @@ __host__ __device__ constexpr unsigned long long fault_code(unsigned role, unsig
            ((unsigned long long)tile << 16);
 }
 
+// Split-K workspace of one stream: fp32 partial tiles and one uint32
+// counter per split tile (each counter is back at zero after every launch).
+// Launches on one stream run in order, so they may share it; launches on
+// different streams may overlap and get different workspaces.
+struct Workspace {
+    cudaStream_t stream = nullptr;
+    float *ws = nullptr;
+    size_t ws_bytes = 0;
+    unsigned *counters = nullptr;
+    size_t counters_n = 0;
+};
+
 // Per-device library state, created on the first call on a device.
 struct DeviceState {
     int device = -1;
     int sm_count = 0;
     unsigned long long *fault_word = nullptr;  // device, 8 bytes
-    // split-K workspace: fp32 partial tiles, then one uint32 counter per tile
-    float *splitk_ws = nullptr;
-    size_t splitk_ws_bytes = 0;
-    unsigned *splitk_counters = nullptr;
-    size_t splitk_counters_n = 0;
+    std::vector<std::unique_ptr<Workspace>> workspaces;  // one per stream used
 };
 
 // Returns the state of the current device (creating it), or an error.
 int device_state(DeviceState **out);
 
-// Grows the split-K workspace of `st` to hold ws_bytes of partials and n
-// counters (zeroed).  Synchronous; only called outside the hot loop.
-int ensure_splitk_workspace(DeviceState *st, size_t ws_bytes, size_t n_counters);
+// The workspace of `stream` on st's device, grown to hold ws_bytes of
+// partials and n_counters counters (new counters zeroed).  Growing
+// synchronises the device; it happens only when a launch needs more than
+// any earlier one on that stream.
+int stream_workspace(DeviceState *st, cudaStream_t stream, size_t ws_bytes, size_t n_counters,
+                     Workspace **out);
 
 struct RuntimeConfig {
     int64_t watchdog_ms;
@@ -85,6 +98,17 @@ bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
 
 // ---- kernel launchers (return cudaSuccess or the launch error) ----
 
+// Operand layouts and fused epilogue of the *_ex entry points (host side):
+// trans_a: A stored K x M; trans_b: B stored N x K; bias: nullptr or N
+// values (fp32 when bias_f32, else bf16); act: a gemm_act_t.  A null
+// GemmOpts pointer means row-major operands and the plain epilogue.
+struct GemmOpts {
+    int trans_a, trans_b;
+    const void *bias;
+    int bias_f32;
+    int act;
+};
+
 cudaError_t launch_sgemm_simt(int M, int N, int K, float alpha, const float *A, int64_t lda,
                               const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
                               cudaStream_t stream);
@@ -93,14 +117,15 @@ cudaError_t launch_sgemm_simt(int M, int N, int K, float alpha, const float *A, 
 // multiples of 4.  Returns a gemm_status_t.
 int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const float *A,
                      int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
-                     cudaStream_t stream);
+                     const GemmOpts *opts, cudaStream_t stream);
 
-// Generic SIMT GEMM for any alignment; a_bf16/b_bf16 select bf16 operands,
-// c_f32 selects an fp32 (else bf16) C.
+// Generic SIMT GEMM for any alignment and layout; bf16_in selects bf16
+// operands, c_f32 selects an fp32 (else bf16) C.  K == 0 (with any A, B)
+// gives C = act(bias) + beta * C.
 cudaError_t launch_gemm_simt_generic(int M, int N, int K, float alpha, const void *A,
                                      int64_t lda, const void *B, int64_t ldb, float beta,
                                      void *C, int64_t ldc, bool bf16_in, bool c_f32,
-                                     cudaStream_t stream);
+                                     const GemmOpts *opts, cudaStream_t stream);
 
 // C = beta * C (C = 0 without reading it when beta == 0).
 cudaError_t launch_scale_c(int M, int N, float beta, void *C, int64_t ldc, bool c_f32,
@@ -111,6 +136,12 @@ cudaError_t launch_scale_c(int M, int N, float beta, void *C, int64_t ldc, bool 
 int validate_gemm_args(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_t lda,
                        size_t a_esz, const void *B, int64_t ldb, size_t b_esz, float beta,
                        const void *C, int64_t ldc, size_t c_esz);
+// The same with stored layouts: trans_a means A is stored K x M (lda >=
+// max(1, M)), trans_b that B is stored N x K (ldb >= max(1, K)).
+int validate_gemm_args_ex(int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+                          int64_t lda, size_t a_esz, bool trans_a, const void *B, int64_t ldb,
+                          size_t b_esz, bool trans_b, float beta, const void *C, int64_t ldc,
+                          size_t c_esz);
 
 // Split-K storage supplied by the caller instead of the library workspace.
 struct ExternalScratch {
@@ -126,12 +157,14 @@ struct ExternalScratch {
 int launch_bf16_tcgen05_external(int device, int sm_count, const ExternalScratch &ext, int M,
                                  int N, int K, float alpha, const uint16_t *A, int64_t lda,
                                  const uint16_t *B, int64_t ldb, float beta, void *C,
-                                 int64_t ldc, bool c_f32, cudaStream_t stream);
+                                 int64_t ldc, bool c_f32, const GemmOpts *opts,
+                                 cudaStream_t stream);
 
 // BF16 tcgen05 GEMM.  Requires 16-byte aligned A/B bases and lda, ldb
-// multiples of 8.  Returns a gemm_status_t.
+// multiples of 8 (in whichever layout opts selects).  Returns a
+// gemm_status_t.
 int launch_bf16_tcgen05(DeviceState *st, int M, int N, int K, float alpha, const uint16_t *A,
                         int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,
-                        int64_t ldc, bool c_f32, cudaStream_t stream);
+                        int64_t ldc, bool c_f32, const GemmOpts *opts, cudaStream_t stream);
 
 }  // namespace gemm

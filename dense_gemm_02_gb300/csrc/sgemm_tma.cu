@@ -1,4 +1,5 @@
-// FP32 SGEMM on the CUDA cores fed by TMA: C = alpha * A * B + beta * C.
+// FP32 SGEMM on the CUDA cores fed by TMA: C = alpha * A * B + beta * C, with
+// the optional fused bias / activation epilogue of epilogue.cuh.
 //
 // Same method as sgemm_simt.cu ("CUDA hand-written SGEMM: 0.4 -> 10.23
 // TFLOPS" (gtnt.cn): shared-memory tiling with a sliding K window, bank-
@@ -31,6 +32,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "internal.h"
 #include "ptx_sm100.cuh"
 
@@ -55,6 +57,12 @@ struct TmaParams {
     int num_m_blk, num_n_blk;
     unsigned long long *fault_word;
     unsigned long long timeout_ns;
+    EpiParams epi;  // bias / activation of the fused epilogue
+    // Partial-wave K split: blocks past tiles_main take one K slice
+    // (kt_per_split 32-deep steps) of a tile split `splits` ways.
+    int tiles_main, splits, kt_per_split;
+    float *ws;           // fp32 partial tiles of the split tiles
+    unsigned *counters;  // one per split tile
 };
 
 __global__ void __launch_bounds__(TTHREADS, 2)
@@ -64,16 +72,27 @@ __global__ void __launch_bounds__(TTHREADS, 2)
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + TOFF_BAR);
     volatile int *never = reinterpret_cast<volatile int *>(full + TSTAGES);
+    volatile int *last_slice = never + 1;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 2, wn = warp & 3;  // 2 x 4 warps, warp tile 64 x 32
     const int tm = lane >> 2, tn = lane & 3;  // 8 x 4 threads, thread tile 8 x 8
 
+    // Blocks 0..tiles_main-1 compute whole tiles; each later block one K
+    // slice of a tile of the partial last wave.
+    int tile = blockIdx.x, slice = -1;
+    if (tile >= p.tiles_main) {
+        const int v = tile - p.tiles_main;
+        tile = p.tiles_main + v / p.splits;
+        slice = v - (v / p.splits) * p.splits;
+    }
     int m_blk, n_blk;
-    grouped_tile_coords(blockIdx.x, p.num_m_blk, p.num_n_blk, kRasterGroup, m_blk, n_blk);
+    grouped_tile_coords(tile, p.num_m_blk, p.num_n_blk, kRasterGroup, m_blk, n_blk);
     const int m0 = m_blk * TBM, n0 = n_blk * TBN;
-    const int KT = (p.K + TBK - 1) / TBK;
+    const int KT_all = (p.K + TBK - 1) / TBK;
+    const int kt0 = slice < 0 ? 0 : slice * p.kt_per_split;
+    const int KT = slice < 0 ? KT_all : min(p.kt_per_split, KT_all - kt0);  // >= 1
 
     if (tid == 0) {
         for (int s = 0; s < TSTAGES; ++s) mbar_init(&full[s], 1);
@@ -88,8 +107,8 @@ __global__ void __launch_bounds__(TTHREADS, 2)
         const int s = kt % TSTAGES;
         uint8_t *st = smem + s * TSTAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], TSTAGE_BYTES);
-        tma_load_2d(st, &tmA, &full[s], kt * TBK, m0);
-        tma_load_2d(st + TA_BYTES, &tmB, &full[s], n0, kt * TBK);
+        tma_load_2d(st, &tmA, &full[s], (kt0 + kt) * TBK, m0);
+        tma_load_2d(st + TA_BYTES, &tmB, &full[s], n0, (kt0 + kt) * TBK);
     };
     int issued = 0;
     if (tid == 0)
@@ -168,8 +187,54 @@ __global__ void __launch_bounds__(TTHREADS, 2)
         return;
     }
 
-    // Epilogue: C = alpha * acc + beta * C (C unread when beta == 0); row
-    // wm*64 + tm + 8i, columns wn*32 + tn*4 + {0..3} and +16.
+    if (slice >= 0) {
+        // Split tile: store this slice's partial sums (thread-major float4
+        // columns, coalesced), count the slice in, and let the last slice to
+        // arrive add all slices in the fixed order 0..splits-1, so the result
+        // does not depend on which slice finishes last.
+        const size_t split_tile = (size_t)(tile - p.tiles_main);
+        float4 *base = reinterpret_cast<float4 *>(p.ws) + split_tile * p.splits * (16 * TTHREADS);
+        float4 *mine = base + (size_t)slice * (16 * TTHREADS);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                __stcg(mine + (2 * i + h) * TTHREADS + tid,
+                       make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
+                                   acc[i][4 * h + 3]));
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned old = atomicAdd(&p.counters[split_tile], 1u);
+            *last_slice = (old == (unsigned)(p.splits - 1)) ? 1 : 0;
+        }
+        __syncthreads();
+        if (!*last_slice) return;
+        __threadfence();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float4 v = __ldcg(base + (2 * i + h) * TTHREADS + tid);
+#pragma unroll 1
+                for (int sl = 1; sl < p.splits; ++sl) {
+                    const float4 w = __ldcg(base + ((size_t)sl * 16 + 2 * i + h) * TTHREADS + tid);
+                    v.x += w.x;
+                    v.y += w.y;
+                    v.z += w.z;
+                    v.w += w.w;
+                }
+                acc[i][4 * h] = v.x;
+                acc[i][4 * h + 1] = v.y;
+                acc[i][4 * h + 2] = v.z;
+                acc[i][4 * h + 3] = v.w;
+            }
+        if (tid == 0) p.counters[split_tile] = 0u;  // ready for the next launch
+    }
+
+    // Epilogue: C = act(alpha * acc + bias) + beta * C (C unread when
+    // beta == 0; without bias and activation fmaf(alpha, acc, beta * C));
+    // row wm*64 + tm + 8i, columns wn*32 + tn*4 + {0..3} and +16.
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int row = m0 + wm * 64 + tm + 8 * i;
@@ -178,28 +243,30 @@ __global__ void __launch_bounds__(TTHREADS, 2)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = n0 + wn * 32 + tn * 4 + 16 * h;
+            if (col >= p.N) continue;
+            const bool vec = p.c_vec && col + 3 < p.N;
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            if (p.beta != 0.f) {
+                if (vec) {
+                    const float4 cv = *reinterpret_cast<const float4 *>(crow + col);
+                    c[0] = cv.x, c[1] = cv.y, c[2] = cv.z, c[3] = cv.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (col + j < p.N) c[j] = crow[col + j];
+                }
+            }
             float v[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = p.alpha * acc[i][4 * h + j];
-            if (p.c_vec && col + 3 < p.N) {
-                float4 *dst = reinterpret_cast<float4 *>(crow + col);
-                if (p.beta != 0.f) {
-                    const float4 c = *dst;
-                    v[0] = fmaf(p.alpha, acc[i][4 * h + 0], p.beta * c.x);
-                    v[1] = fmaf(p.alpha, acc[i][4 * h + 1], p.beta * c.y);
-                    v[2] = fmaf(p.alpha, acc[i][4 * h + 2], p.beta * c.z);
-                    v[3] = fmaf(p.alpha, acc[i][4 * h + 3], p.beta * c.w);
-                }
-                *dst = make_float4(v[0], v[1], v[2], v[3]);
+            for (int j = 0; j < 4; ++j)
+                v[j] = epi_finish(p.epi, p.alpha, p.beta, acc[i][4 * h + j],
+                                  col + j < p.N ? col + j : p.N - 1, c[j]);
+            if (vec) {
+                *reinterpret_cast<float4 *>(crow + col) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    if (col + j < p.N) {
-                        if (p.beta != 0.f)
-                            v[j] = fmaf(p.alpha, acc[i][4 * h + j], p.beta * crow[col + j]);
-                        crow[col + j] = v[j];
-                    }
-                }
+                for (int j = 0; j < 4; ++j)
+                    if (col + j < p.N) crow[col + j] = v[j];
             }
         }
     }
@@ -209,7 +276,7 @@ __global__ void __launch_bounds__(TTHREADS, 2)
 
 int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const float *A,
                      int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
-                     cudaStream_t stream) {
+                     const GemmOpts *opts, cudaStream_t stream) {
     static bool attr_done[kMaxDevices] = {};
     if (!attr_done[st->device]) {
         if (cudaFuncSetAttribute(sgemm_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -223,7 +290,13 @@ int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const fl
         !encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, (uint64_t)N, (uint64_t)K,
                               (uint64_t)ldb * 4, TBN, TBK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return GEMM_ERR_CUDA;
-    TmaParams p;
+    TmaParams p{};
+    if (opts) {
+        p.epi.bias = opts->bias;
+        p.epi.bias_f32 = opts->bias_f32 ? 1 : 0;
+        p.epi.act = opts->act;
+        p.epi.on = (opts->bias != nullptr || opts->act != 0) ? 1 : 0;
+    }
     p.M = M;
     p.N = N;
     p.K = K;
@@ -238,7 +311,57 @@ int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const fl
     p.timeout_ns = (unsigned long long)runtime_config().watchdog_ms * 1000000ull;
     const long long tiles = (long long)p.num_m_blk * p.num_n_blk;
     if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
-    sgemm_tma_kernel<<<(unsigned)tiles, TTHREADS, TSMEM_ALLOC, stream>>>(ta, tb, p);
+
+    // Partial last wave.  The kernel is bound by the FP32 pipe, so an SM
+    // finishes its tiles at about the same rate whether one or two CTAs
+    // share it: what counts is the work per SM.  After the first
+    // tiles - rem tiles (rem = tiles mod SMs) every SM has had the same
+    // share; the last rem tiles would put one more whole tile on rem SMs
+    // while the others idle.  Each of them is split along K into S slices
+    // (at least four 32-deep K steps each, S <= 8) with S chosen to minimise
+    // the busiest SM's extra work, ceil(rem * S / SMs) / S of a tile; the
+    // slices meet in a workspace.  (4096^3 on 152 SMs: rem 112, S = 4, 0.75
+    // of a tile instead of 1.)
+    p.tiles_main = (int)tiles;
+    p.splits = 1;
+    p.kt_per_split = 0;
+    p.ws = nullptr;
+    p.counters = nullptr;
+    const int KT = (K + TBK - 1) / TBK;
+    const long long sms = st->sm_count;
+    if (!runtime_config().tail_split_off && sms > 0) {
+        const long long rem = tiles % sms;
+        int best = 1;
+        double best_t = rem ? 1.0 : 0.0;
+        for (int S = 2; S <= 8 && S <= KT / 4 && rem; ++S) {
+            const double t = (double)((rem * S + sms - 1) / sms) / S;
+            if (t < best_t - 0.02) {
+                best_t = t;
+                best = S;
+            }
+        }
+        if (best >= 2) {
+            const int per = (KT + best - 1) / best;
+            const int splits = (KT + per - 1) / per;  // no empty slice
+            if (splits >= 2) {
+                p.tiles_main = (int)(tiles - rem);
+                p.splits = splits;
+                p.kt_per_split = per;
+            }
+        }
+    }
+    const long long split_tiles = tiles - p.tiles_main;
+    const long long units = p.tiles_main + split_tiles * p.splits;
+    if (units > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    if (split_tiles > 0) {
+        Workspace *w = nullptr;
+        const size_t ws_bytes = (size_t)split_tiles * p.splits * TBM * TBN * sizeof(float);
+        const int rc = stream_workspace(st, stream, ws_bytes, (size_t)split_tiles, &w);
+        if (rc != GEMM_OK) return rc;
+        p.ws = w->ws;
+        p.counters = w->counters;
+    }
+    sgemm_tma_kernel<<<(unsigned)units, TTHREADS, TSMEM_ALLOC, stream>>>(ta, tb, p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

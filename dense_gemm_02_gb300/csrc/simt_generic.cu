@@ -1,10 +1,12 @@
 // Generic GPU paths that accept any pitch and any element alignment:
-//   * gemm_simt_generic: C = alpha*A*B + beta*C with fp32 or bf16 operands
-//     and an fp32 or bf16 C, on the CUDA cores with fp32 accumulation.  It
-//     serves BF16 inputs whose rows cannot be fetched by TMA (pitch not a
-//     multiple of 8 elements, or a base that is not 16-byte aligned).  The
-//     product of two bf16 values is exact in fp32, so the arithmetic is the
-//     same fp32 accumulation as on the tensor cores, in another order.
+//   * gemm_simt_generic: C = act(alpha*op(A)*op(B) + bias) + beta*C with
+//     fp32 or bf16 operands in either layout (op(X) = X or X^T) and an fp32
+//     or bf16 C, on the CUDA cores with fp32 accumulation.  It serves BF16
+//     inputs whose rows cannot be fetched by TMA (pitch not a multiple of 8
+//     elements, or a base that is not 16-byte aligned) and FP32 operands in
+//     transposed layouts.  The product of two bf16 values is exact in fp32,
+//     so the arithmetic is the same fp32 accumulation as on the tensor
+//     cores, in another order.
 //   * scale_c: C = beta * C for alpha == 0 or K == 0 (C is written without
 //     being read when beta == 0).
 // The tiling follows the plain shared-memory scheme of "CUDA shared memory
@@ -16,6 +18,7 @@
 
 #include <cstdint>
 
+#include "epilogue.cuh"
 #include "internal.h"
 
 namespace gemm {
@@ -30,6 +33,8 @@ struct GenericParams {
     const void *B;
     void *C;
     long long lda, ldb, ldc;
+    int trans_a, trans_b;  // A stored K x M / B stored N x K
+    EpiParams epi;
 };
 
 template <bool BF16>
@@ -79,19 +84,23 @@ __global__ void __launch_bounds__(GTHREADS) gemm_simt_generic_kernel(const Gener
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int idx = tid + GTHREADS * i;  // 0..1023
+            // Consecutive threads take consecutive addresses of whichever
+            // index is contiguous in memory.
             {
-                const int k = idx & 15, m = idx >> 4;
+                const int k = p.trans_a ? idx >> 6 : idx & 15;
+                const int m = p.trans_a ? idx & 63 : idx >> 4;
                 const int gm = m0 + m, gk = k0 + k;
-                As[k][m] = (gm < p.M && gk < p.K)
-                               ? load_in<BF16IN>(p.A, (long long)gm * p.lda + gk)
-                               : 0.f;
+                const long long off =
+                    p.trans_a ? (long long)gk * p.lda + gm : (long long)gm * p.lda + gk;
+                As[k][m] = (gm < p.M && gk < p.K) ? load_in<BF16IN>(p.A, off) : 0.f;
             }
             {
-                const int n = idx & 63, k = idx >> 6;
+                const int n = p.trans_b ? idx >> 4 : idx & 63;
+                const int k = p.trans_b ? idx & 15 : idx >> 6;
                 const int gk = k0 + k, gn = n0 + n;
-                Bs[k][n] = (gk < p.K && gn < p.N)
-                               ? load_in<BF16IN>(p.B, (long long)gk * p.ldb + gn)
-                               : 0.f;
+                const long long off =
+                    p.trans_b ? (long long)gn * p.ldb + gk : (long long)gk * p.ldb + gn;
+                Bs[k][n] = (gk < p.K && gn < p.N) ? load_in<BF16IN>(p.B, off) : 0.f;
             }
         }
         __syncthreads();
@@ -118,9 +127,8 @@ __global__ void __launch_bounds__(GTHREADS) gemm_simt_generic_kernel(const Gener
             const int col = n0 + tx + 16 * j;
             if (col >= p.N) continue;
             const long long idx = (long long)row * p.ldc + col;
-            float v = p.alpha * acc[i][j];
-            if (p.beta != 0.f) v = fmaf(p.alpha, acc[i][j], p.beta * load_c<F32OUT>(p.C, idx));
-            store_c<F32OUT>(p.C, idx, v);
+            const float c = (p.beta != 0.f) ? load_c<F32OUT>(p.C, idx) : 0.f;
+            store_c<F32OUT>(p.C, idx, epi_finish(p.epi, p.alpha, p.beta, acc[i][j], col, c));
         }
     }
 }
@@ -142,8 +150,16 @@ __global__ void scale_c_kernel(int M, int N, float beta, void *C, long long ldc)
 cudaError_t launch_gemm_simt_generic(int M, int N, int K, float alpha, const void *A,
                                      int64_t lda, const void *B, int64_t ldb, float beta,
                                      void *C, int64_t ldc, bool bf16_in, bool c_f32,
-                                     cudaStream_t stream) {
-    GenericParams p{M, N, K, alpha, beta, A, B, C, lda, ldb, ldc};
+                                     const GemmOpts *opts, cudaStream_t stream) {
+    GenericParams p{M, N, K, alpha, beta, A, B, C, lda, ldb, ldc, 0, 0, EpiParams{}};
+    if (opts) {
+        p.trans_a = opts->trans_a ? 1 : 0;
+        p.trans_b = opts->trans_b ? 1 : 0;
+        p.epi.bias = opts->bias;
+        p.epi.bias_f32 = opts->bias_f32 ? 1 : 0;
+        p.epi.act = opts->act;
+        p.epi.on = (opts->bias != nullptr || opts->act != 0) ? 1 : 0;
+    }
     const int nm = (M + GB - 1) / GB, nn = (N + GB - 1) / GB;
     const long long tiles = (long long)nm * nn;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;

@@ -39,9 +39,11 @@
  * before anything is launched; GEMM_ERR_CUDA means a CUDA call failed at
  * launch.  Device-side faults of the pipeline (a wait that ran past its
  * time limit) are recorded in a per-device status word that
- * gemm_get_device_status() returns.  The library keeps one small piece of
- * per-device state (the status word and, for split-K launches, a workspace
- * it allocates on first use); gemm_shutdown() frees it.
+ * gemm_get_device_status() returns.  The library keeps a little
+ * per-device state: the status word and, for launches that split K, one
+ * fp32 workspace per stream, allocated on first use and grown (which
+ * synchronises the device) when a launch needs more than any before it on
+ * that stream; gemm_shutdown() frees it.
  *
  * Thread safety: calls may come from several host threads; each call only
  * reads shared configuration.
@@ -66,11 +68,12 @@ typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = -1,        /* negative size, unknown enum, bad key */
     GEMM_ERR_NULLPTR = -2,            /* a matrix that must be read/written is NULL */
-    GEMM_ERR_BAD_LD = -3,             /* lda < max(1,K), ldb < max(1,N) or ldc < max(1,N) */
+    GEMM_ERR_BAD_LD = -3,             /* lda < max(1,K), ldb < max(1,N) or ldc < max(1,N)
+                                         (transposed operands: lda < max(1,M), ldb < max(1,K)) */
     GEMM_ERR_UNSUPPORTED_DEVICE = -4, /* current device is not compute capability 10.3 */
     GEMM_ERR_CUDA = -5,               /* a CUDA runtime/driver call failed */
     GEMM_ERR_DEVICE_TIMEOUT = -6,     /* a pipeline wait on the GPU ran out of time */
-    GEMM_ERR_ALIAS = -7,              /* C overlaps A or B */
+    GEMM_ERR_ALIAS = -7,              /* C overlaps A, B or the bias */
     GEMM_ERR_TOO_LARGE = -8,          /* a dimension or pitch exceeds 2^31 - 1 */
     GEMM_ERR_SCRATCH_LIMIT = -9       /* gemm_bf16_noalloc: the call needs more split-K
                                          scratch than its static maximum */
@@ -114,6 +117,57 @@ GEMM_API int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha,
 GEMM_API int gemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
               const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
               float beta, void *C, int64_t ldc, int c_type, void *stream);
+
+/* Activation of the fused epilogue. */
+typedef enum {
+    GEMM_ACT_NONE = 0,
+    GEMM_ACT_RELU = 1,      /* max(x, 0) */
+    GEMM_ACT_GELU_TANH = 2  /* 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+} gemm_act_t;
+
+/*
+ * Options of the extended entry points: operand layouts and a fused
+ * epilogue.  A zero-initialised struct means "no transposes, no epilogue".
+ *   trans_a    0: A is M x K row-major (lda >= K);
+ *              1: the caller stores A^T, K x M row-major (lda >= M)
+ *   trans_b    0: B is K x N row-major (ldb >= N);
+ *              1: the caller stores B^T, N x K row-major (ldb >= K)
+ *   bias       NULL, or a device vector of N values added to every row
+ *   bias_type  GEMM_OUT_BF16 or GEMM_OUT_F32: element type of bias
+ *   act        gemm_act_t
+ */
+typedef struct {
+    int trans_a;
+    int trans_b;
+    const void *bias;
+    int bias_type;
+    int act;
+} gemm_opts_t;
+
+/*
+ * Extended GEMMs with transposed operands and a fused epilogue:
+ *     C = act(alpha * op(A) * op(B) + bias) + beta * C
+ * op(X) is X or, with trans_x, the transpose of the stored matrix.  The
+ * activation comes first and beta * C (a residual) is added after it, the
+ * order of the fused "GELU, then residual add" kernel of the "Z-Turbo"
+ * tuning page (lanjinlin.com.cn), section 2.1; "Blackwell BF16 GEMM ..."
+ * (lshu.cn), section 3.3, names GELU and residual as epilogue fusions, and
+ * section 5.1 the transposed GEMMs of training.  The epilogue runs in fp32:
+ * v = act(fmaf(alpha, acc, bias)), then out = v + beta * C with beta * C
+ * rounded first (as in the plain epilogue fmaf(alpha, acc, beta * C)), then
+ * the single conversion to C's type.  opts == NULL (or all zero) gives
+ * exactly gemm_bf16 / gemm_f32.  Same memory, stream and error rules as the
+ * plain entry points; additionally bias must not overlap C
+ * (GEMM_ERR_ALIAS), and an unknown act or bias_type is GEMM_ERR_INVALID_ARG.
+ */
+GEMM_API int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, float alpha,
+                          const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
+                          float beta, void *C, int64_t ldc, int c_type,
+                          const gemm_opts_t *opts, void *stream);
+GEMM_API int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha,
+                         const float *A, int64_t lda, const float *B, int64_t ldb,
+                         float beta, float *C, int64_t ldc, const gemm_opts_t *opts,
+                         void *stream);
 
 /*
  * Allocation-free BF16 GEMM.  The source pages have no counterpart: this is

@@ -93,6 +93,39 @@ def test_argument_errors_are_reported_before_any_cuda_call(lib):
              None) == b.GEMM_ERR_ALIAS
 
 
+def test_extended_entry_point_errors(lib):
+    """gemm_bf16_ex / gemm_f32_ex: option and layout checks run before any
+    CUDA call (the stored shapes of transposed operands set the pitch
+    minimums, and the bias may not overlap C)."""
+    from dense_gemm_02_gb300 import binding as b
+
+    fake = 1 << 20
+    for f, extra in ((b.gemm_bf16_ex, (b.GEMM_OUT_F32,)), (b.gemm_f32_ex, ())):
+        def call(M, N, K, lda, ldb, ldc, opts, A=fake, B=fake + 65536, C=fake + 131072):
+            return f(M, N, K, 1.0, A, lda, B, ldb, 0.0, C, ldc, *extra, opts, None)
+
+        # unknown activation, bias type or transpose flag
+        assert call(4, 4, 4, 4, 4, 4, b.make_opts(act=3)) == b.GEMM_ERR_INVALID_ARG
+        assert call(4, 4, 4, 4, 4, 4, b.make_opts(act=-1)) == b.GEMM_ERR_INVALID_ARG
+        assert call(4, 4, 4, 4, 4, 4, b.make_opts(bias_type=5)) == b.GEMM_ERR_INVALID_ARG
+        bad = b.make_opts()
+        bad.trans_a = 2
+        assert call(4, 4, 4, 4, 4, 4, bad) == b.GEMM_ERR_INVALID_ARG
+        # trans_a: A stored K x M needs lda >= M; trans_b: B stored N x K
+        # needs ldb >= K
+        ta, tb = b.make_opts(trans_a=True), b.make_opts(trans_b=True)
+        assert call(8, 4, 2, 4, 4, 4, ta) == b.GEMM_ERR_BAD_LD      # lda 4 < M 8
+        assert call(2, 4, 8, 4, 4, 4, tb) == b.GEMM_ERR_BAD_LD      # ldb 4 < K 8
+        # C overlapping a transposed A (stored K x M = 16 x 4, pitch 4: at
+        # least 128 bytes; row-major it would be rejected as lda < K)
+        assert call(4, 4, 16, 4, 4, 4, ta, A=fake, C=fake + 100) == b.GEMM_ERR_ALIAS
+        # bias overlapping C
+        ob = b.make_opts(bias=fake + 131072 + 8)
+        assert call(4, 4, 4, 4, 4, 4, ob) == b.GEMM_ERR_ALIAS
+        # empty output: nothing to do, no pointer needed
+        assert f(0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, *extra, ta, None) == b.GEMM_OK
+
+
 def test_config_keys(lib):
     from dense_gemm_02_gb300 import binding as b
 
@@ -105,7 +138,7 @@ def test_config_keys(lib):
     with pytest.raises(b.GemmError):
         b.set_config("bf16_tile_n", 96)
     assert b.last_kernel() in {"none", "sgemm_simt", "sgemm_tma", "bf16_tcgen05", "bf16_simt",
-                                "scale_c"}
+                                "f32_simt", "scale_c"}
 
 
 def test_package_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -135,6 +135,42 @@ def test_f32_tma_and_cp_async_kernels_agree_exactly(force):
     assert C.guards_intact()
 
 
+# Shapes whose tile count leaves a remainder over the SM count, so the
+# FP32 kernel splits the remaining tiles along K (on 152 SMs: 2304^2 has 324
+# tiles, 20 past two full rounds, split 4 ways at K = 520; 1000^2 has 64,
+# all split; 4096 x 4096 has 1024, 112 split 4 ways).  tail_split_off = 1
+# runs the same shapes unsplit.
+@pytest.mark.parametrize("M,N,K", [(2304, 2304, 520), (1000, 1000, 1000), (4096, 4096, 520),
+                                   (1001, 1003, 999)])
+@pytest.mark.parametrize("tail_off", [0, 1])
+def test_f32_partial_wave_k_split_integer(M, N, K, tail_off):
+    seed = 8800 + M + N + K
+    A = gi.draw("integer", seed, 0, (M, K))
+    B = gi.draw("integer", seed, 1, (K, N))
+    Cin = gi.draw("integer", seed, 2, (M, N))
+    g.set_config("tail_split_off", tail_off)
+    try:
+        C = run_f32(A, B, Cin, 0.5, -1.0, lda=K + (-K) % 4, ldb=N + (-N) % 4)
+    finally:
+        g.set_config("tail_split_off", 0)
+    assert g.binding.last_kernel() == "sgemm_tma"
+    ref = oracle.round_f32(oracle.gemm(A, B, Cin, alpha=0.5, beta=-1.0))
+    got = C.result()
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} mismatches"
+    assert C.guards_intact()
+
+
+def test_f32_partial_wave_k_split_uniform_tolerance_and_repeatable():
+    M, N, K = 2304, 2304, 1032
+    A = gi.draw("uniform", 8900, 0, (M, K))
+    B = gi.draw("uniform", 8900, 1, (K, N))
+    C1 = run_f32(A, B, None, 1.0, 0.0)
+    C2 = run_f32(A, B, None, 1.0, 0.0)
+    assert np.array_equal(C1.result(), C2.result())
+    ref = oracle.gemm(A, B)
+    assert np.abs(C1.result().astype(np.float64) - ref).max() <= 1e-5 * K
+
+
 def test_f32_alpha_zero_and_k_zero_scale_c():
     M, N, K = 70, 90, 33
     A = np.full((M, K), np.nan, np.float32)
