@@ -60,6 +60,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--variant", default="plain",
+                    help="operand layouts and fused epilogue of the extended entry points, "
+                         "comma-separated: a layout nn|tn|nt|tt (t: that operand stored "
+                         "transposed), 'bias' (N fp32 values), an activation relu|gelu; "
+                         "'plain' = the plain entry points")
     ap.add_argument("--config", action="append", default=[], metavar="KEY=VALUE",
                     help="library tuning knob (gemm_set_config), may repeat")
     return ap.parse_args()
@@ -285,6 +290,7 @@ def config_block(workloads, args):
         "host_ahead": "the GPU idles ~100 us before each step (outside the timed events) so "
                       "kernel events exclude host launch overhead",
         "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU",
+        "variant": getattr(args, "variant", "plain"),
         "library_config": list(getattr(args, "config", [])),
     }
 
@@ -316,6 +322,22 @@ def recorded_traffic(w):
     return rec.get("dram_bytes_per_launch")
 
 
+def parse_variant(spec):
+    """(trans_a, trans_b, bias, act) of a --variant string."""
+    ta = tb = False
+    bias, act = False, "none"
+    for tok in [t for t in spec.split(",") if t and t != "plain"]:
+        if tok in ("nn", "tn", "nt", "tt"):
+            ta, tb = tok[0] == "t", tok[1] == "t"
+        elif tok == "bias":
+            bias = True
+        elif tok in ("relu", "gelu"):
+            act = tok
+        else:
+            raise SystemExit(f"unknown --variant item {tok!r}")
+    return ta, tb, bias, act
+
+
 def run_ours(args, dist):
     import torch
 
@@ -330,7 +352,13 @@ def run_ours(args, dist):
     for kv in args.config:
         key, val = kv.split("=", 1)
         g.set_config(key, int(val))
+    import gemm_inputs as gi
+
     workloads = workloads_for(args.workload)
+    v_ta, v_tb, v_bias, v_act = parse_variant(args.variant)
+    extended = args.variant != "plain"
+    if extended:
+        args.no_e2e = True  # the host-buffer API runs the plain entry points
     peaks, peak_src = load_peaks()
     props = torch.cuda.get_device_properties(dist.local_rank)
     sms = props.multi_processor_count
@@ -352,16 +380,26 @@ def run_ours(args, dist):
         else:
             hC = None
         dA, dB = hA.cuda(), hB.cuda()
+        # Transposed storage: the same logical operand, held K x M (or N x
+        # K) row-major; the library reads that layout in place.
+        if v_ta:
+            dA = dA.t().contiguous().t()
+        if v_tb:
+            dB = dB.t().contiguous().t()
         dC = hC.cuda() if hC is not None else torch.empty((w.M, w.N), dtype=out_dt,
                                                             device="cuda")
-        dev_ops.append((w, dA, dB, dC))
+        bias = (torch.from_numpy(gi.draw("normal", 0xB1A5 + w.index, 3, (w.N,))).cuda()
+                if v_bias else None)
+        dev_ops.append((w, dA, dB, dC, bias))
         host_ops.append((w, hA.pin_memory(), hB.pin_memory(),
                          hC.pin_memory() if hC is not None else None, out_dt))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def launch(w, dA, dB, dC):
-        if w.dtype == "f32":
+    def launch(w, dA, dB, dC, bias):
+        if extended:
+            g.gemm_ex(dA, dB, dC, alpha=w.alpha, beta=w.beta, bias=bias, act=v_act)
+        elif w.dtype == "f32":
             g.sgemm(dA, dB, dC, alpha=w.alpha, beta=w.beta)
         else:
             g.gemm_bf16(dA, dB, dC, alpha=w.alpha, beta=w.beta)
@@ -416,21 +454,21 @@ def run_ours(args, dist):
                  "achieved_gbs_min_bytes": gbs}
         if w.dtype == "f32":
             rl = {"bound": "alu", "achieved": tflops, "peak": fp32_peak, "unit": "TFLOP/s",
-                  "frac": tflops / fp32_peak, "traffic": recorded_traffic(w),
+                  "frac": tflops / fp32_peak, "traffic": None if extended else recorded_traffic(w),
                   "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
                                  f"x {sm_max:.0f} MHz (max SM clock)",
                   "kernel": kernel_name(w)}
         elif w.M * w.N * w.K / (w.min_bytes() / 2) < 300:  # intensity below the ridge: HBM
             peak_bw = peaks["hbm_gbs"]
             rl = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
-                  "frac": gbs / peak_bw, "traffic": recorded_traffic(w),
+                  "frac": gbs / peak_bw, "traffic": None if extended else recorded_traffic(w),
                   "peak_source": f"{peak_src} hbm_gbs",
                   "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
                   "kernel": kernel_name(w)}
         else:
             pk = peaks["bf16_tflops"]
             rl = {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s",
-                  "frac": tflops / pk, "traffic": recorded_traffic(w),
+                  "frac": tflops / pk, "traffic": None if extended else recorded_traffic(w),
                   "peak_source": f"{peak_src} bf16_tflops (burst)",
                   "frac_of_sustained": tflops / peaks.get("bf16_tflops_sustained", pk),
                   "kernel": kernel_name(w)}

@@ -33,13 +33,21 @@ __device__ __forceinline__ float epi_bias(const EpiParams &e, int col) {
     return __uint_as_float(static_cast<uint32_t>(bits) << 16);
 }
 
+// GELU, tanh form, through the identity 0.5 (1 + tanh(u)) = 1 / (1 + e^-2u):
+//     gelu(x) = x / (1 + exp(-2u)),  u = sqrt(2/pi) (x + 0.044715 x^3)
+// (no cancellation for negative x, and one exponential instead of a tanh).
+// expf is CUDA's (2 ulp); __fdividef returns 0 once 1 + e^-2u passes 2^126,
+// where the quotient is below any fp32 value of interest anyway.
+__device__ __forceinline__ float gelu_tanh(float x) {
+    const float u = 0.7978845608028654f * fmaf(0.044715f * x * x, x, x);
+    return __fdividef(x, 1.f + expf(-2.f * u));
+}
+
+__device__ __forceinline__ float relu(float v) { return v > 0.f ? v : 0.f; }  // -0, NaN -> +0
+
 __device__ __forceinline__ float epi_act(int act, float v) {
-    if (act == 1) return v > 0.f ? v : 0.f;  // relu; -0 and NaN give +0
-    if (act == 2) {
-        // 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))
-        const float u = 0.7978845608028654f * fmaf(0.044715f * v * v, v, v);
-        return 0.5f * v * (1.f + tanhf(u));
-    }
+    if (act == 1) return relu(v);
+    if (act == 2) return gelu_tanh(v);
     return v;
 }
 

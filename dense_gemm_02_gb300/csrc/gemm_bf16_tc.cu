@@ -470,10 +470,49 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
 
 // Fused epilogue, first part: v[j] = act(alpha * v[j] + bias[gn + j]) for
 // the 32 columns gn..gn+31 (columns past N use bias[N - 1]; they are never
-// stored).  The store helpers then add beta * C with alpha = 1.
+// stored).  The store helpers then add beta * C with alpha = 1.  The bias
+// chunk is read with 16-byte loads when it is aligned and inside N; the
+// activation is chosen once per chunk, so each unrolled loop holds one form.
 __device__ __forceinline__ void apply_pre(const TcParams &p, int gn, float (&v)[32]) {
+    const float alpha = p.alpha;
+    if (p.epi.bias) {
+        float b[32];
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(p.epi.bias);
+        if (gn + 32 <= p.N && p.epi.bias_f32 && (addr & 15) == 0) {
+            const float4 *src = static_cast<const float4 *>(p.epi.bias) + (gn >> 2);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = epi_pre(p.epi, p.alpha, v[j], min(gn + j, p.N - 1));
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = __ldg(src + q);
+                b[4 * q] = x.x, b[4 * q + 1] = x.y, b[4 * q + 2] = x.z, b[4 * q + 3] = x.w;
+            }
+        } else if (gn + 32 <= p.N && !p.epi.bias_f32 && (addr & 15) == 0) {
+            const uint4 *src = static_cast<const uint4 *>(p.epi.bias) + (gn >> 3);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 x = __ldg(src + q);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    b[8 * q + e] = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u)
+                                                           : (w[e >> 1] << 16));
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) b[j] = epi_bias(p.epi, min(gn + j, p.N - 1));
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = fmaf(alpha, v[j], b[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= alpha;
+    }
+    if (p.epi.act == 2) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_tanh(v[j]);
+    } else if (p.epi.act == 1) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = relu(v[j]);
+    }
 }
 
 // EPI: the fused bias / activation epilogue is compiled in (a separate
