@@ -23,6 +23,7 @@ std::atomic<int64_t> g_bf16_tile_n{0};
 std::atomic<int64_t> g_tail_split_off{0};
 std::atomic<int64_t> g_raster_group{0};
 std::atomic<int64_t> g_cta_pair{0};
+std::atomic<int64_t> g_stream_k{0};
 std::atomic<int64_t> g_last_fault{0};
 
 std::mutex g_state_mu;
@@ -146,7 +147,7 @@ int stream_workspace(DeviceState *st, cudaStream_t stream, size_t ws_bytes, size
 RuntimeConfig runtime_config() {
     return RuntimeConfig{g_watchdog_ms.load(), g_force_path.load(), g_fault_inject.load(),
                          g_split_k.load(),      g_bf16_tile_n.load(), g_tail_split_off.load(),
-                         g_raster_group.load(), g_cta_pair.load()};
+                         g_raster_group.load(), g_cta_pair.load(), g_stream_k.load()};
 }
 
 void consume_fault_inject() { g_fault_inject.store(0); }
@@ -396,6 +397,9 @@ extern "C" int gemm_set_config(const char *key, int64_t value) {
     } else if (!strcmp(key, "cta_pair")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
         g_cta_pair.store(value);
+    } else if (!strcmp(key, "stream_k")) {
+        if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+        g_stream_k.store(value);
     } else {
         return GEMM_ERR_INVALID_ARG;
     }
@@ -412,6 +416,7 @@ extern "C" int gemm_get_config(const char *key, int64_t *value) {
     else if (!strcmp(key, "tail_split_off")) *value = g_tail_split_off.load();
     else if (!strcmp(key, "raster_group")) *value = g_raster_group.load();
     else if (!strcmp(key, "cta_pair")) *value = g_cta_pair.load();
+    else if (!strcmp(key, "stream_k")) *value = g_stream_k.load();
     else return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }

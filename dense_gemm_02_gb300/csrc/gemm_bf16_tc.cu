@@ -34,6 +34,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -80,6 +81,12 @@ struct TcParams {
     int M, N, K;
     int num_m_blk, num_n_blk, num_kb;
     int splits, kb_per_split;
+    // Stream-K (single-CTA kernel): the tiles' K iterations, tiles * num_kb
+    // in tile-major order, are cut into gridDim.x contiguous ranges of equal
+    // length, one per CTA; a tile shared by several CTAs is summed in a
+    // workspace with up to max_parts slices per tile.
+    int stream_k;
+    int max_parts;
     int num_units;
     int group_m;     // M-blocks per raster band
     int tiles_main;  // tiles run at full width; the rest are split along N
@@ -150,9 +157,11 @@ __device__ __forceinline__ OperandLayout operand_layout(int mn_major) {
 }
 
 // One unit of work: output rows m_blk*128.., columns n0..n0+width-1, K
-// blocks kb0..kb1-1.  `tile` indexes the full-width tile (split-K counters).
+// blocks kb0..kb1-1.  `tile` indexes the full-width tile (split-K counters);
+// the tile's K range is shared by `nparts` units, this one being number
+// `part` in K order (nparts == 1: the unit owns the whole tile).
 struct Unit {
-    int tile, m_blk, n0, width, kb0, kb1, split;
+    int tile, m_blk, n0, width, kb0, kb1, part, nparts;
 };
 
 // Unit order: split-K launches enumerate (tile, slice); otherwise the first
@@ -163,10 +172,11 @@ template <int BN>
 __device__ __forceinline__ Unit decode_unit(const TcParams &p, int u) {
     Unit r;
     int sub = 0, nsub = 1;
-    r.split = 0;
+    r.part = 0;
+    r.nparts = p.splits;
     if (p.splits > 1) {
         r.tile = u / p.splits;
-        r.split = u - r.tile * p.splits;
+        r.part = u - r.tile * p.splits;
     } else if (u < p.tiles_main) {
         r.tile = u;
     } else {
@@ -179,9 +189,47 @@ __device__ __forceinline__ Unit decode_unit(const TcParams &p, int u) {
     grouped_tile_coords(r.tile, p.num_m_blk, p.num_n_blk, p.group_m, r.m_blk, n_blk);
     r.width = BN / nsub;
     r.n0 = n_blk * BN + sub * r.width;
-    r.kb0 = r.split * p.kb_per_split;
+    r.kb0 = r.part * p.kb_per_split;
     r.kb1 = min(r.kb0 + p.kb_per_split, p.num_kb);
     return r;
+}
+
+// Stream-K: the CTA that owns K iteration x of the tile-major sequence of
+// T = tiles * num_kb iterations cut into P ranges [c*T/P, (c+1)*T/P).
+__device__ __forceinline__ long long sk_owner(long long x, long long P, long long T) {
+    return ((x + 1) * P - 1) / T;
+}
+
+// The i-th unit this CTA works on (false: none left).  Persistent mode:
+// units blockIdx.x, blockIdx.x + gridDim.x, ...  Stream-K: the i-th piece
+// of this CTA's iteration range, cut at tile boundaries.
+template <int BN>
+__device__ __forceinline__ bool cta_unit(const TcParams &p, int i, Unit &w) {
+    if (!p.stream_k) {
+        const long long u = (long long)blockIdx.x + (long long)i * gridDim.x;
+        if (u >= p.num_units) return false;
+        w = decode_unit<BN>(p, (int)u);
+        return true;
+    }
+    const long long P = gridDim.x, nkb = p.num_kb;
+    const long long T = (long long)p.num_units * nkb;  // num_units = tiles here
+    const long long c = blockIdx.x;
+    const long long s = c * T / P, e = (c + 1) * T / P;
+    const long long t0 = s / nkb;
+    const long long t = t0 + i;
+    const long long pos = (i == 0) ? s : t * nkb;
+    if (pos >= e) return false;
+    w.tile = (int)t;
+    w.kb0 = (int)(pos - t * nkb);
+    w.kb1 = (int)min(nkb, e - t * nkb);
+    const long long first = sk_owner(t * nkb, P, T), last = sk_owner(t * nkb + nkb - 1, P, T);
+    w.part = (int)(c - first);
+    w.nparts = (int)(last - first + 1);
+    int n_blk;
+    grouped_tile_coords(w.tile, p.num_m_blk, p.num_n_blk, p.group_m, w.m_blk, n_blk);
+    w.width = BN;
+    w.n0 = n_blk * BN;
+    return true;
 }
 
 __device__ __forceinline__ void record_fault(const TcParams &p, volatile int *abort_flag,
@@ -424,8 +472,8 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
     uint32_t it = 0;
     int withheld = -1;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<BN>(p, u);
+    Unit w;
+    for (int ui = 0; ok && cta_unit<BN>(p, ui, w); ++ui) {
         if (w.n0 >= p.N) continue;  // sub-tile wholly past the N edge
         const int boxes = w.width / 64;
         const uint32_t tx = Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES;
@@ -601,8 +649,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t b1 = lb.step, b2 = 2 * lb.step, b3 = 3 * lb.step;
             uint32_t s = 0, ph = 0, local = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-                const Unit w = decode_unit<BN>(p, u);
+            Unit w;
+            for (int ui = 0; ok && cta_unit<BN>(p, ui, w); ++ui) {
                 if (w.n0 >= p.N) continue;
                 const uint32_t idesc = idesc_bf16_f32(w.width, TC_BM, p.a_mn, p.b_kmaj);
                 const uint32_t b = local & 1u, use = local >> 1;
@@ -651,8 +699,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         uint8_t *warp_stage = smem + Cfg::OFF_STAGE + q * 2 * kEpiChunkBytes;
         uint32_t stage_seq = 0;
         uint32_t local = 0;
-        for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-            const Unit w = decode_unit<BN>(p, u);
+        Unit w;
+        for (int ui = 0; cta_unit<BN>(p, ui, w); ++ui) {
             if (w.n0 >= p.N) continue;
             const int tile = w.tile;
             const uint32_t b = local & 1u, use = local >> 1;
@@ -671,7 +719,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
             const int gm = w.m_blk * TC_BM + row;
             const int gn0 = w.n0;
-            if (p.splits == 1) {
+            if (w.nparts == 1) {
 #pragma unroll 1
                 for (int c = 0; c < w.width / 32; ++c) {
                     uint32_t r[32];
@@ -691,8 +739,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tc_fence_before_sync();
                 mbar_arrive(&tempty[b]);
             } else {
-                const int split = w.split;
-                float *wrow = p.ws + (((size_t)tile * p.splits + split) * TC_BM + row) * BN;
+                float *wrow = p.ws + (((size_t)tile * p.max_parts + w.part) * TC_BM + row) * BN;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
@@ -714,7 +761,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 named_bar_sync(TC_EPI_BAR, TC_EPI_THREADS);
                 if (et == 0) {
                     const unsigned old = atomicAdd(&p.counters[tile], 1u);
-                    *last_flag = (old == (unsigned)(p.splits - 1)) ? 1 : 0;
+                    *last_flag = (old == (unsigned)(w.nparts - 1)) ? 1 : 0;
                 }
                 named_bar_sync(TC_EPI_BAR, TC_EPI_THREADS);
                 if (*last_flag) {
@@ -724,7 +771,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     __threadfence();
                     const int rows = min(TC_BM, p.M - w.m_blk * TC_BM);
                     const int c4n = BN / 4;
-                    const float *base = p.ws + (size_t)tile * p.splits * TC_BM * BN;
+                    const float *base = p.ws + (size_t)tile * p.max_parts * TC_BM * BN;
                     const size_t slice = (size_t)TC_BM * BN;
                     // Four elements per thread per pass and up to four slices
                     // per step keep 16 independent loads in flight.
@@ -746,7 +793,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         }
                         int sl = 1;
 #pragma unroll 1
-                        for (; sl + 3 < p.splits; sl += 4) {
+                        for (; sl + 3 < w.nparts; sl += 4) {
                             float4 x[4][4];
 #pragma unroll
                             for (int t = 0; t < 4; ++t)
@@ -765,7 +812,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 }
                         }
 #pragma unroll 1
-                        for (; sl < p.splits; ++sl) {
+                        for (; sl < w.nparts; ++sl) {
                             float4 x[4];
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
@@ -1196,9 +1243,22 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
     const long long tiles = (long long)p.num_m_blk * p.num_n_blk;
     int splits = 1;
     const RuntimeConfig cfg = runtime_config();
+    // Few tiles (at most half the SMs) and a long K: split K.  By default
+    // into equal slices per tile (as many as keep the SMs busy); with
+    // `stream_k` set, stream-K instead: all tiles * num_kb K iterations are
+    // dealt out to P CTAs in equal contiguous ranges (P = SMs, at least 4
+    // iterations each), so every SM streams the same number of operand
+    // bytes whatever the tile count.  (Measured on GB300, 64 x 8192 x 8192:
+    // equal slices 42 us, stream-K 46 us; its tiles are shared by up to
+    // four CTAs and the extra partial tiles cost more than the balance
+    // gains.)
+    const bool small = tiles * 2 <= sm_count && p.num_kb >= 8;
+    long long sk_ctas = 0;
     if (cfg.split_k > 0) {
         splits = (int)cfg.split_k;
-    } else if (tiles * 2 <= sm_count && p.num_kb >= 8) {
+    } else if (small && cfg.stream_k) {
+        sk_ctas = std::min<long long>(sm_count, tiles * p.num_kb / 4);
+    } else if (small) {
         splits = (int)(sm_count / tiles);
         if (splits > p.num_kb / 4) splits = p.num_kb / 4;
     }
@@ -1240,14 +1300,32 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
             p.tail_split = (int)f;
         }
     }
-    const long long units = (p.splits > 1) ? tiles * p.splits
-                                           : p.tiles_main + (tiles - p.tiles_main) * p.tail_split;
+    long long units = (p.splits > 1) ? tiles * p.splits
+                                     : p.tiles_main + (tiles - p.tiles_main) * p.tail_split;
+    p.stream_k = 0;
+    p.max_parts = p.splits;
+    if (sk_ctas > 1) {
+        // Largest number of CTAs sharing one tile (each tile's first and
+        // last iterations' owners, as the kernel computes them).
+        const long long T = tiles * p.num_kb;
+        long long mp = 1;
+        for (long long t = 0; t < tiles; ++t) {
+            const long long first = ((t * p.num_kb + 1) * sk_ctas - 1) / T;
+            const long long last = ((t * p.num_kb + p.num_kb) * sk_ctas - 1) / T;
+            mp = std::max(mp, last - first + 1);
+        }
+        p.stream_k = 1;
+        p.max_parts = (int)mp;
+        p.tiles_main = (int)tiles;
+        p.tail_split = 1;
+        units = tiles;  // the kernel deals out num_units * num_kb iterations
+    }
     if (units > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
     p.num_units = (int)units;
     p.ws = nullptr;
     p.counters = nullptr;
-    if (p.splits > 1) {
-        const size_t ws_bytes = (size_t)units * TC_BM * BN * sizeof(float);
+    if (p.splits > 1 || p.stream_k) {
+        const size_t ws_bytes = (size_t)tiles * p.max_parts * TC_BM * BN * sizeof(float);
         if (ext) {
             if (ws_bytes > ext->ws_bytes || (size_t)tiles > ext->counters_n)
                 return GEMM_ERR_SCRATCH_LIMIT;
@@ -1266,7 +1344,7 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
             p.counters = w->counters;
         }
     }
-    const int grid = (int)(units < sm_count ? units : sm_count);
+    const int grid = p.stream_k ? (int)sk_ctas : (int)(units < sm_count ? units : sm_count);
     if (p.epi.on)
         bf16_tc_kernel<BN, true><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, tc, p);
     else

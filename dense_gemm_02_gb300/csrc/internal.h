@@ -66,6 +66,7 @@ struct RuntimeConfig {
     int64_t tail_split_off;
     int64_t raster_group;
     int64_t cta_pair;
+    int64_t stream_k;
 };
 RuntimeConfig runtime_config();
 void consume_fault_inject();

@@ -236,7 +236,11 @@ GEMM_API const char *gemm_status_string(int status);
  *   "split_k"       0 auto, else the number of K slices for the tcgen05 kernel
  *   "bf16_tile_n"   0 auto, else 128 or 256 (tcgen05 tile width)
  *   "tail_split_off" 1: do not cut the tiles of the last partial wave into
- *                   narrower sub-tiles (tcgen05 kernel); 0 (default) cuts them
+ *                   narrower sub-tiles (tcgen05 kernel) or along K (FP32
+ *                   TMA kernel); 0 (default) cuts them
+ *   "stream_k"      1: when a tcgen05 GEMM has few tiles and a long K, deal
+ *                   all K iterations out to the SMs in equal ranges
+ *                   (stream-K); 0 (default): equal K slices per tile
  *   "raster_group"  0 auto, else the number of M-blocks (128 rows, or 256
  *                   for CTA pairs) per raster band of the tcgen05 kernel
  *   "cta_pair"      0 auto, 1 single-CTA tcgen05 kernel only, 2 always the

@@ -254,6 +254,43 @@ def test_bf16_tiles_and_split_k_integer(tile_n, split_k):
     assert C.guards_intact()
 
 
+# Few tiles and a long K: with stream_k = 1 the K iterations of all tiles
+# are dealt out to the SMs in equal ranges (tiles shared by 2-4 CTAs, summed
+# in K order); stream_k = 0 (default) runs equal K slices per tile.
+@pytest.mark.parametrize("M,N,K", [(64, 8192, 2048), (1, 1000, 4096), (200, 520, 3000),
+                                   (129, 264, 1000), (7, 72, 8192), (64, 2048, 8200)])
+@pytest.mark.parametrize("stream_k", [0, 1])
+def test_bf16_stream_k_integer(M, N, K, stream_k):
+    seed = 6600 + M + N + K
+    A = gi.draw("integer", seed, 0, (M, K), dtype="bf16")
+    B = gi.draw("integer", seed, 1, (K, N), dtype="bf16")
+    Cin = gi.draw("integer", seed, 2, (M, N), dtype="f32")
+    g.set_config("stream_k", stream_k)
+    try:
+        C = run_bf16(A, B, Cin, 0.5, 1.0, "f32")
+    finally:
+        g.set_config("stream_k", 0)
+    assert g.binding.last_kernel() == "bf16_tcgen05"
+    ref = oracle.round_f32(oracle.gemm(A, B, Cin, alpha=0.5, beta=1.0))
+    got = C.result()
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} mismatches"
+    assert C.guards_intact()
+
+
+def test_bf16_stream_k_normal_tolerance_and_repeatable():
+    M, N, K = 64, 8192, 8192
+    A = gi.draw("normal", 6700, 0, (M, K), dtype="bf16")
+    B = gi.draw("normal", 6700, 1, (K, N), sigma=0.02, dtype="bf16")
+    g.set_config("stream_k", 1)
+    try:
+        C1 = run_bf16(A, B, None, 1.0, 0.0, "f32")
+        C2 = run_bf16(A, B, None, 1.0, 0.0, "f32")
+    finally:
+        g.set_config("stream_k", 0)
+    assert np.array_equal(C1.result(), C2.result())
+    assert bf16_tolerance_violations(widen(C1.result(), "f32"), oracle.gemm(A, B)) == 0
+
+
 # Tile counts that leave a partial last wave on a 152-SM part, so the tail
 # tiles are cut into 2 or 4 narrower sub-tiles; the ragged-N shape puts
 # sub-tiles wholly past the N edge.
