@@ -7,10 +7,10 @@ bias / activation epilogue.  This package is the thin Python binding.
 """
 
 from . import binding
-from .api import gemm, gemm_bf16, gemm_ex, sgemm
+from .api import gemm, gemm_batched, gemm_bf16, gemm_ex, sgemm
 from .binding import GemmError, get_config, set_config
 
-__all__ = ["gemm", "gemm_bf16", "gemm_ex", "sgemm", "binding", "GemmError", "get_config",
+__all__ = ["gemm", "gemm_batched", "gemm_bf16", "gemm_ex", "sgemm", "binding", "GemmError", "get_config",
            "set_config", "flops"]
 
 

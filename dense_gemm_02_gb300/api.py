@@ -3,7 +3,8 @@
 ``sgemm`` and ``gemm_bf16`` take CUDA tensors (row-major, unit column
 stride) and enqueue one library call on the current torch stream.
 ``gemm_ex`` adds transposed operands (a ``X.t()`` view is read in place)
-and the fused bias / activation epilogue.
+and the fused bias / activation epilogue; ``gemm_batched`` runs a strided
+batch of such products in one launch.
 ``gemm`` additionally accepts host (CPU) tensors: it copies them to the
 device, runs the same call and copies C back, which is the end-to-end path
 a caller holding host buffers uses.  Nothing here computes: shapes, strides
@@ -116,6 +117,74 @@ def gemm_ex(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
                          float(beta), C.data_ptr(), _row_major(C, "C"), c_type, opts,
                          _stream_handle(stream))
     _b.check(rc, "gemm_bf16_ex")
+    return C
+
+
+def gemm_batched(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
+                 alpha: float = 1.0, beta: float = 0.0, bias: torch.Tensor | None = None,
+                 act: str = "none", out_dtype=None, stream=None) -> torch.Tensor:
+    """C[i] = act(alpha * A[i] @ B[i] + bias) + beta * C[i] for every i, in one
+    launch (strided batched GEMM).
+
+    A (batch x M x K) and B (batch x K x N) are CUDA tensors whose matrices
+    are each row-major or a transposed view; a batch dimension of size 1 (or
+    stride 0, as from ``expand``) shares that operand among all products.
+    C is batch x M x N with row-major matrices.  Dtypes and ``bias`` /
+    ``act`` as in ``gemm_ex``."""
+    if A.dim() != 3 or B.dim() != 3:
+        raise ValueError("A and B must be 3-D (batch x rows x cols)")
+    if A.dtype != B.dtype or A.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("A and B must both be float32 or both bfloat16")
+    if not (A.is_cuda and B.is_cuda):
+        raise TypeError("A and B must be CUDA tensors")
+    if act not in _ACTS:
+        raise ValueError(f"act must be one of {sorted(_ACTS)}")
+    batch = max(A.size(0), B.size(0))
+    for name, t in (("A", A), ("B", B)):
+        if t.size(0) not in (1, batch):
+            raise ValueError(f"{name} has batch {t.size(0)}, expected 1 or {batch}")
+    M, N, K = _shapes(A[0], B[0], None)
+    ta, lda = _layout(A[0], "A")
+    tb, ldb = _layout(B[0], "B")
+    stride_a = A.stride(0) if A.size(0) > 1 else 0
+    stride_b = B.stride(0) if B.size(0) > 1 else 0
+    bias_ptr, bias_type = None, _b.GEMM_OUT_F32
+    if bias is not None:
+        if bias.dim() != 1 or bias.numel() != N or not bias.is_cuda or not bias.is_contiguous():
+            raise ValueError(f"bias must be a contiguous CUDA vector of {N} values")
+        if bias.dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError("bias must be float32 or bfloat16")
+        bias_type = _b.GEMM_OUT_F32 if bias.dtype == torch.float32 else _b.GEMM_OUT_BF16
+        bias_ptr = bias.data_ptr()
+    opts = _b.make_opts(ta, tb, bias_ptr, bias_type, _ACTS[act])
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs an input C")
+        od = torch.float32 if A.dtype == torch.float32 else (out_dtype or torch.bfloat16)
+        C = torch.empty((batch, M, N), dtype=od, device=A.device)
+    if C.dim() != 3 or tuple(C.shape) != (batch, M, N) or not C.is_cuda:
+        raise ValueError(f"C must be a CUDA tensor of shape {(batch, M, N)}")
+    ldc = _row_major(C[0], "C")
+    stride_c = C.stride(0) if batch > 1 else max(1, M * ldc)
+    h = _stream_handle(stream)
+    if A.dtype == torch.float32:
+        if C.dtype != torch.float32:
+            raise TypeError("C must be float32 for float32 operands")
+        rc = _b.gemm_f32_batched(batch, M, N, K, float(alpha), A.data_ptr(), lda, stride_a,
+                                 B.data_ptr(), ldb, stride_b, float(beta), C.data_ptr(), ldc,
+                                 stride_c, opts, h)
+        _b.check(rc, "gemm_f32_batched")
+        return C
+    if C.dtype == torch.bfloat16:
+        c_type = _b.GEMM_OUT_BF16
+    elif C.dtype == torch.float32:
+        c_type = _b.GEMM_OUT_F32
+    else:
+        raise TypeError("C must be bfloat16 or float32")
+    rc = _b.gemm_bf16_batched(batch, M, N, K, float(alpha), A.data_ptr(), lda, stride_a,
+                              B.data_ptr(), ldb, stride_b, float(beta), C.data_ptr(), ldc, stride_c,
+                              c_type, opts, h)
+    _b.check(rc, "gemm_bf16_batched")
     return C
 
 

@@ -53,6 +53,10 @@ SIGNATURES = {
                             ctypes.POINTER(GemmOpts), _vp]),
     "gemm_f32_ex": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                            ctypes.POINTER(GemmOpts), _vp]),
+    "gemm_bf16_batched": (_int, [_i64, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64, _i64,
+                                 _f32, _vp, _i64, _i64, _int, ctypes.POINTER(GemmOpts), _vp]),
+    "gemm_f32_batched": (_int, [_i64, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64, _i64,
+                                _f32, _vp, _i64, _i64, ctypes.POINTER(GemmOpts), _vp]),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_get_device_fault_info": (_i64, []),
     "gemm_status_string": (_cp, [_int]),
@@ -142,6 +146,22 @@ def gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, opts, stream) -> i
     """Raw call of the extended FP32 GEMM; opts is a GemmOpts or None."""
     ptr = ctypes.byref(opts) if opts is not None else None
     return lib().gemm_f32_ex(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ptr, stream)
+
+
+def gemm_bf16_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, beta, C, ldc,
+                      stride_c, c_type, opts, stream) -> int:
+    """Raw call of the strided batched BF16 GEMM; opts is a GemmOpts or None."""
+    ptr = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_bf16_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,
+                                   beta, C, ldc, stride_c, c_type, ptr, stream)
+
+
+def gemm_f32_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, beta, C, ldc,
+                     stride_c, opts, stream) -> int:
+    """Raw call of the strided batched FP32 GEMM; opts is a GemmOpts or None."""
+    ptr = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_f32_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,
+                                  beta, C, ldc, stride_c, ptr, stream)
 
 
 def get_device_status(stream=None) -> int:

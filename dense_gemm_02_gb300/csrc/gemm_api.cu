@@ -162,7 +162,7 @@ namespace {
 // Checks the public options and converts them.  A NULL opts gives the
 // plain layouts and epilogue.
 int convert_opts(const gemm_opts_t *opts, GemmOpts *out) {
-    *out = GemmOpts{0, 0, nullptr, 0, GEMM_ACT_NONE};
+    *out = GemmOpts{};
     if (!opts) return GEMM_OK;
     if ((opts->trans_a != 0 && opts->trans_a != 1) || (opts->trans_b != 0 && opts->trans_b != 1))
         return GEMM_ERR_INVALID_ARG;
@@ -181,6 +181,56 @@ int convert_opts(const gemm_opts_t *opts, GemmOpts *out) {
 
 bool has_epilogue(const GemmOpts &o) { return o.bias != nullptr || o.act != GEMM_ACT_NONE; }
 
+// Strided-batch checks, after the per-matrix ones: non-negative strides; C
+// matrices that do not overlap one another; C clear of every A, B and bias
+// byte the batch reads.
+int check_batch(const GemmOpts &o, int64_t M, int64_t N, int64_t K, float alpha, const void *A,
+                int64_t lda, size_t a_esz, const void *B, int64_t ldb, size_t b_esz,
+                const void *C, int64_t ldc, size_t c_esz) {
+    if (o.batch <= 1) return GEMM_OK;
+    if (o.stride_a < 0 || o.stride_b < 0 || o.stride_c < 0) return GEMM_ERR_INVALID_ARG;
+    if (o.batch > kMaxDim || o.stride_a > (int64_t(1) << 40) || o.stride_b > (int64_t(1) << 40) ||
+        o.stride_c > (int64_t(1) << 40))
+        return GEMM_ERR_TOO_LARGE;
+    const size_t c_one = span_bytes(M, N, ldc, c_esz);
+    if ((size_t)o.stride_c * c_esz < c_one) return GEMM_ERR_ALIAS;  // C matrices overlap
+    const size_t c_all = (size_t)(o.batch - 1) * o.stride_c * c_esz + c_one;
+    if (alpha != 0.f && K > 0) {
+        const int64_t a_rows = o.trans_a ? K : M, a_cols = o.trans_a ? M : K;
+        const int64_t b_rows = o.trans_b ? N : K, b_cols = o.trans_b ? K : N;
+        const size_t a_all = (size_t)(o.batch - 1) * o.stride_a * a_esz +
+                             span_bytes(a_rows, a_cols, lda, a_esz);
+        const size_t b_all = (size_t)(o.batch - 1) * o.stride_b * b_esz +
+                             span_bytes(b_rows, b_cols, ldb, b_esz);
+        if (ranges_overlap(C, c_all, A, a_all) || ranges_overlap(C, c_all, B, b_all))
+            return GEMM_ERR_ALIAS;
+    }
+    if (o.bias && ranges_overlap(C, c_all, o.bias, (size_t)N * (o.bias_f32 ? 4 : 2)))
+        return GEMM_ERR_ALIAS;
+    return GEMM_OK;
+}
+
+// Whether A and B (in their stored layouts, over the batch) can be fetched by
+// TMA: 16-byte aligned bases, pitches and batch strides that are multiples
+// of 16 bytes.
+bool tma_operands_ok(const GemmOpts &o, int64_t M, int64_t N, int64_t K, const void *A,
+                     int64_t lda, const void *B, int64_t ldb, size_t esz) {
+    const int64_t q = 16 / (int64_t)esz;
+    if ((reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15) ||
+        lda % q || ldb % q)
+        return false;
+    const int64_t a_rows = o.trans_a ? K : M, b_rows = o.trans_b ? N : K;
+    return tma_batch_stride_ok(o.batch, o.stride_a * (int64_t)esz, a_rows * lda * (int64_t)esz) &&
+           tma_batch_stride_ok(o.batch, o.stride_b * (int64_t)esz, b_rows * ldb * (int64_t)esz);
+}
+
+// The same options for a launch that reads neither A nor B.
+GemmOpts without_ab(const GemmOpts &o) {
+    GemmOpts r = o;
+    r.stride_a = r.stride_b = 0;
+    return r;
+}
+
 // Shared by the plain and extended FP32 entry points.
 int run_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
             const float *B, int64_t ldb, float beta, float *C, int64_t ldc, const GemmOpts &o,
@@ -195,6 +245,8 @@ int run_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_
     if (o.bias && ranges_overlap(C, span_bytes(M, N, ldc, 4), o.bias,
                                  (size_t)N * (o.bias_f32 ? 4 : 2)))
         return GEMM_ERR_ALIAS;
+    if ((rc = check_batch(o, M, N, K, alpha, A, lda, 4, B, ldb, 4, C, ldc, 4)) != GEMM_OK)
+        return rc;
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != GEMM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -202,22 +254,21 @@ int run_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_
     cudaError_t e;
     if (alpha == 0.f || K == 0) {
         if (!epi) {
-            e = launch_scale_c((int)M, (int)N, beta, C, ldc, true, s);
+            e = launch_scale_c((int)M, (int)N, beta, C, ldc, true, o.batch, o.stride_c, s);
             set_last_kernel("scale_c");
         } else {  // act(bias) + beta * C: the generic kernel with an empty K loop
+            const GemmOpts oc = without_ab(o);
             e = launch_gemm_simt_generic((int)M, (int)N, 0, alpha, nullptr, 1, nullptr, 1, beta,
-                                         C, ldc, false, true, &o, s);
+                                         C, ldc, false, true, &oc, s);
             set_last_kernel("f32_simt");
         }
         return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
-    // TMA needs 16-byte aligned bases and pitches that are multiples of 16
-    // bytes (4 floats).  Row-major operands take the TMA kernel (or the
-    // cp.async kernel without an epilogue); transposed ones, and misaligned
-    // ones with an epilogue, the generic kernel.
-    const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
-                        ((reinterpret_cast<uintptr_t>(B) & 15) == 0) && (lda % 4 == 0) &&
-                        (ldb % 4 == 0);
+    // TMA needs 16-byte aligned bases and pitches (and batch strides) that
+    // are multiples of 16 bytes (4 floats).  Row-major operands take the
+    // TMA kernel (or, one matrix without an epilogue, the cp.async kernel);
+    // transposed ones, and others, the generic kernel.
+    const bool tma_ok = tma_operands_ok(o, M, N, K, A, lda, B, ldb, 4);
     const bool row_major = !o.trans_a && !o.trans_b;
     if (row_major && tma_ok && runtime_config().force_path != 1) {
         rc = launch_sgemm_tma(st, (int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C, ldc,
@@ -225,7 +276,7 @@ int run_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_
         if (rc == GEMM_OK) set_last_kernel("sgemm_tma");
         return rc;
     }
-    if (row_major && !epi) {
+    if (row_major && !epi && o.batch == 1) {
         e = launch_sgemm_simt((int)M, (int)N, (int)K, alpha, A, lda, B, ldb, beta, C, ldc, s);
         set_last_kernel("sgemm_simt");
     } else {
@@ -253,26 +304,28 @@ int run_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A, in
     if (o.bias && ranges_overlap(C, span_bytes(M, N, ldc, c_esz), o.bias,
                                  (size_t)N * (o.bias_f32 ? 4 : 2)))
         return GEMM_ERR_ALIAS;
+    if ((rc = check_batch(o, M, N, K, alpha, A, lda, 2, B, ldb, 2, C, ldc, c_esz)) != GEMM_OK)
+        return rc;
     DeviceState *st = nullptr;
     if ((rc = device_state(&st)) != GEMM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (alpha == 0.f || K == 0) {
         cudaError_t e;
         if (!has_epilogue(o)) {
-            e = launch_scale_c((int)M, (int)N, beta, C, ldc, c_f32, s);
+            e = launch_scale_c((int)M, (int)N, beta, C, ldc, c_f32, o.batch, o.stride_c, s);
             set_last_kernel("scale_c");
         } else {  // act(bias) + beta * C: the generic kernel with an empty K loop
+            const GemmOpts oc = without_ab(o);
             e = launch_gemm_simt_generic((int)M, (int)N, 0, alpha, nullptr, 1, nullptr, 1, beta,
-                                         C, ldc, true, c_f32, &o, s);
+                                         C, ldc, true, c_f32, &oc, s);
             set_last_kernel("bf16_simt");
         }
         return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
-    // TMA needs 16-byte aligned bases and row pitches that are multiples of
-    // 16 bytes (8 bf16 elements), in either stored layout.
-    const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&
-                        ((reinterpret_cast<uintptr_t>(B) & 15) == 0) && (lda % 8 == 0) &&
-                        (ldb % 8 == 0);
+    // TMA needs 16-byte aligned bases and row pitches (and batch strides)
+    // that are multiples of 16 bytes (8 bf16 elements), in either stored
+    // layout.
+    const bool tma_ok = tma_operands_ok(o, M, N, K, A, lda, B, ldb, 2);
     const int64_t force = runtime_config().force_path;
     if (force == 2 && !tma_ok) return GEMM_ERR_INVALID_ARG;
     if (tma_ok && force != 1) {
@@ -324,6 +377,45 @@ extern "C" int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, float alpha, const 
     const int rc = convert_opts(opts, &o);
     if (rc != GEMM_OK) return rc;
     return run_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, o, stream);
+}
+
+extern "C" int gemm_bf16_batched(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha,
+                                 const uint16_t *A, int64_t lda, int64_t stride_a,
+                                 const uint16_t *B, int64_t ldb, int64_t stride_b, float beta,
+                                 void *C, int64_t ldc, int64_t stride_c, int c_type,
+                                 const gemm_opts_t *opts, void *stream) {
+    GemmOpts o;
+    int rc = convert_opts(opts, &o);
+    if (rc != GEMM_OK) return rc;
+    if (batch < 0) return GEMM_ERR_INVALID_ARG;
+    if (batch == 0) {
+        set_last_kernel("none");
+        return GEMM_OK;
+    }
+    o.batch = batch;
+    o.stride_a = stride_a;
+    o.stride_b = stride_b;
+    o.stride_c = stride_c;
+    return run_bf16(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type, o, stream);
+}
+
+extern "C" int gemm_f32_batched(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha,
+                                const float *A, int64_t lda, int64_t stride_a, const float *B,
+                                int64_t ldb, int64_t stride_b, float beta, float *C, int64_t ldc,
+                                int64_t stride_c, const gemm_opts_t *opts, void *stream) {
+    GemmOpts o;
+    int rc = convert_opts(opts, &o);
+    if (rc != GEMM_OK) return rc;
+    if (batch < 0) return GEMM_ERR_INVALID_ARG;
+    if (batch == 0) {
+        set_last_kernel("none");
+        return GEMM_OK;
+    }
+    o.batch = batch;
+    o.stride_a = stride_a;
+    o.stride_b = stride_b;
+    o.stride_c = stride_c;
+    return run_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, o, stream);
 }
 
 extern "C" int gemm_get_device_status(void *stream) {

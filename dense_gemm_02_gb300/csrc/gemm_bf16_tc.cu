@@ -105,6 +105,12 @@ struct TcParams {
     EpiParams epi;  // bias / activation of the fused epilogue
     int a_mn;       // A stored K x M (op(A) = A^T): MN-major A tiles
     int b_kmaj;     // B stored N x K (op(B) = B^T): K-major B tiles
+    // Strided batch: tile t is tile t % tiles_per_batch of matrix
+    // t / tiles_per_batch; a_bmul / b_bmul are 0 for an operand shared by
+    // the whole batch (its TMA batch coordinate stays 0); C matrix i starts
+    // c_bstride elements after C.
+    int tiles_per_batch, a_bmul, b_bmul;
+    long long c_bstride;
 };
 
 // Shared-memory matrix descriptor of tcgen05 (PTX ISA, "matrix descriptor"):
@@ -162,7 +168,13 @@ __device__ __forceinline__ OperandLayout operand_layout(int mn_major) {
 // `part` in K order (nparts == 1: the unit owns the whole tile).
 struct Unit {
     int tile, m_blk, n0, width, kb0, kb1, part, nparts;
+    int bidx;  // matrix of the batch
 };
+
+// C of matrix bidx of the batch.
+__device__ __forceinline__ void *c_matrix(const TcParams &p, int bidx) {
+    return static_cast<char *>(p.C) + (long long)bidx * p.c_bstride * (p.c_f32 ? 4 : 2);
+}
 
 // Unit order: split-K launches enumerate (tile, slice); otherwise the first
 // tiles_main tiles run at full width BN and each remaining tile (the last,
@@ -186,7 +198,9 @@ __device__ __forceinline__ Unit decode_unit(const TcParams &p, int u) {
         nsub = p.tail_split;
     }
     int n_blk;
-    grouped_tile_coords(r.tile, p.num_m_blk, p.num_n_blk, p.group_m, r.m_blk, n_blk);
+    r.bidx = r.tile / p.tiles_per_batch;
+    grouped_tile_coords(r.tile - r.bidx * p.tiles_per_batch, p.num_m_blk, p.num_n_blk, p.group_m,
+                        r.m_blk, n_blk);
     r.width = BN / nsub;
     r.n0 = n_blk * BN + sub * r.width;
     r.kb0 = r.part * p.kb_per_split;
@@ -226,7 +240,9 @@ __device__ __forceinline__ bool cta_unit(const TcParams &p, int i, Unit &w) {
     w.part = (int)(c - first);
     w.nparts = (int)(last - first + 1);
     int n_blk;
-    grouped_tile_coords(w.tile, p.num_m_blk, p.num_n_blk, p.group_m, w.m_blk, n_blk);
+    w.bidx = w.tile / p.tiles_per_batch;
+    grouped_tile_coords(w.tile - w.bidx * p.tiles_per_batch, p.num_m_blk, p.num_n_blk, p.group_m,
+                        w.m_blk, n_blk);
     w.width = BN;
     w.n0 = n_blk * BN;
     return true;
@@ -245,12 +261,13 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
 // Stores 32 consecutive outputs of row gm starting at column gn:
 // C = alpha * acc + beta * C, converted to C's type.  (With the fused
 // epilogue, acc already holds act(alpha * acc + bias) and alpha is 1.)
-__device__ __forceinline__ void store_row_chunk(const TcParams &p, float alpha, int gm, int gn,
+__device__ __forceinline__ void store_row_chunk(const TcParams &p, float alpha, void *C, int gm,
+                                                int gn,
                                                 const float (&acc)[32]) {
     if (gm >= p.M) return;
     const float beta = p.beta;
     if (p.c_f32) {
-        float *crow = static_cast<float *>(p.C) + (long long)gm * p.ldc;
+        float *crow = static_cast<float *>(C) + (long long)gm * p.ldc;
         if (p.c_vec && gn + 32 <= p.N) {
             float4 *dst = reinterpret_cast<float4 *>(crow + gn);
 #pragma unroll
@@ -277,7 +294,7 @@ __device__ __forceinline__ void store_row_chunk(const TcParams &p, float alpha, 
             }
         }
     } else {
-        uint16_t *crow = static_cast<uint16_t *>(p.C) + (long long)gm * p.ldc;
+        uint16_t *crow = static_cast<uint16_t *>(C) + (long long)gm * p.ldc;
         if (p.c_vec && gn + 32 <= p.N) {
             uint4 *dst = reinterpret_cast<uint4 *>(crow + gn);
 #pragma unroll
@@ -323,7 +340,8 @@ __device__ __forceinline__ void store_row_chunk(const TcParams &p, float alpha, 
 // at c ^ (row & 7); bf16 rows of 64 bytes with chunk c at c ^ ((row >> 1) & 3).
 // Stores are asynchronous; a buffer is reused once the store issued two
 // chunks earlier has finished reading it.
-__device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha,
+template <bool B3>
+__device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha, void *C, int bidx,
                                                 const CUtensorMap *tmC,
                                                 uint8_t *warp_stage, uint32_t &seq, int lane,
                                                 int gm0, int gn, const float (&acc)[32]) {
@@ -334,7 +352,7 @@ __device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha,
     for (int j = 0; j < 32; ++j) o[j] = alpha * acc[j];
     if (beta != 0.f && gm < p.M) {
         if (p.c_f32) {
-            const float *crow = static_cast<const float *>(p.C) + (long long)gm * p.ldc + gn;
+            const float *crow = static_cast<const float *>(C) + (long long)gm * p.ldc + gn;
             if (gn + 32 <= p.N) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -350,7 +368,7 @@ __device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha,
                     if (gn + j < p.N) o[j] = fmaf(alpha, acc[j], beta * crow[j]);
             }
         } else {
-            const uint16_t *crow = static_cast<const uint16_t *>(p.C) + (long long)gm * p.ldc + gn;
+            const uint16_t *crow = static_cast<const uint16_t *>(C) + (long long)gm * p.ldc + gn;
             if (gn + 32 <= p.N) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -397,7 +415,12 @@ __device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha,
         // A chunk wholly outside C stores nothing, but still closes a
         // (then empty) group so that the buffer-reuse wait above always
         // refers to the store issued two chunks earlier.
-        if (gm0 < p.M && gn < p.N) tma_store_2d(tmC, buf, gn, gm0);
+        if (gm0 < p.M && gn < p.N) {
+            if constexpr (B3)
+                tma_store_3d(tmC, buf, gn, gm0, bidx);
+            else
+                tma_store_2d(tmC, buf, gn, gm0);
+        }
         bulk_commit_group();
     }
     ++seq;
@@ -406,14 +429,14 @@ __device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha,
 // Stores C[gm][gn..gn+3] = alpha * acc + beta * C (one 16-byte fp32 or
 // 8-byte bf16 store when C rows are 16-byte aligned and the four columns
 // are inside C).
-__device__ __forceinline__ void store_quad(const TcParams &p, float alpha, int gm, int gn,
+__device__ __forceinline__ void store_quad(const TcParams &p, float alpha, void *C, int gm, int gn,
                                            float4 acc) {
     if (gm >= p.M || gn >= p.N) return;
     const float beta = p.beta;
     const float a[4] = {acc.x, acc.y, acc.z, acc.w};
     float o[4];
     if (p.c_f32) {
-        float *crow = static_cast<float *>(p.C) + (long long)gm * p.ldc;
+        float *crow = static_cast<float *>(C) + (long long)gm * p.ldc;
         if (p.c_vec && gn + 4 <= p.N) {
             float4 *dst = reinterpret_cast<float4 *>(crow + gn);
             const float4 c = (beta != 0.f) ? *dst : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -428,7 +451,7 @@ __device__ __forceinline__ void store_quad(const TcParams &p, float alpha, int g
                     crow[gn + j] = beta != 0.f ? fmaf(alpha, a[j], beta * crow[gn + j]) : alpha * a[j];
         }
     } else {
-        uint16_t *crow = static_cast<uint16_t *>(p.C) + (long long)gm * p.ldc;
+        uint16_t *crow = static_cast<uint16_t *>(C) + (long long)gm * p.ldc;
         if (p.c_vec && gn + 4 <= p.N) {
             uint2 *dst = reinterpret_cast<uint2 *>(crow + gn);
             uint2 c = make_uint2(0u, 0u);
@@ -457,12 +480,31 @@ __device__ __forceinline__ void store_quad(const TcParams &p, float alpha, int g
 }
 
 
+// One TMA box of an operand: 3-D maps (B3) take the batch coordinate.
+template <bool B3>
+__device__ __forceinline__ void load_box(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
+                                         int c1, int c2) {
+    if constexpr (B3)
+        tma_load_3d(dst, map, bar, c0, c1, c2);
+    else
+        tma_load_2d(dst, map, bar, c0, c1);
+}
+
+template <bool B3>
+__device__ __forceinline__ void load_box_pair(void *dst, const CUtensorMap *map, uint32_t bar_cl,
+                                              int c0, int c1, int c2) {
+    if constexpr (B3)
+        tma_load_3d_pair(dst, map, bar_cl, c0, c1, c2);
+    else
+        tma_load_2d_pair(dst, map, bar_cl, c0, c1);
+}
+
 // TMA producer of the single-CTA kernel (lane 0 of warp 0) for one operand
 // layout: A_MN, A stored K x M (two 64 (M) x 64 (K) boxes per stage); B_KM,
 // B stored N x K (64 (K) x 64 (N) boxes); else row-major A (one 64 (K) x
 // 128 (M) box) and B (64 (N) x 64 (K) boxes).  Every layout fills a stage
 // with the same bytes.
-template <int BN, bool A_MN, bool B_KM>
+template <int BN, bool A_MN, bool B_KM, bool B3>
 __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap *tmA,
                                             const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
                                             uint64_t *full, uint64_t *empty,
@@ -478,6 +520,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
         const int boxes = w.width / 64;
         const uint32_t tx = Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES;
         const int m0 = w.m_blk * TC_BM;
+        const int ab = w.bidx * p.a_bmul, bb = w.bidx * p.b_bmul;  // batch coordinates
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
             const int s = it % S;
             const uint32_t ph = (it / S) & 1u;
@@ -494,17 +537,19 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
             uint8_t *a_dst = sA + s * Cfg::A_BYTES;
             const int k0 = kb * TC_BK;
             if constexpr (A_MN) {
-                tma_load_2d(a_dst, tmA, &full[s], m0, k0);
-                tma_load_2d(a_dst + 8192, tmA, &full[s], m0 + 64, k0);
+                load_box<B3>(a_dst, tmA, &full[s], m0, k0, ab);
+                load_box<B3>(a_dst + 8192, tmA, &full[s], m0 + 64, k0, ab);
             } else {
-                tma_load_2d(a_dst, tmA, &full[s], k0, m0);
+                load_box<B3>(a_dst, tmA, &full[s], k0, m0, ab);
             }
             uint8_t *b_dst = sB + s * Cfg::B_BYTES;
             for (int j = 0; j < boxes; ++j) {
                 if constexpr (B_KM)
-                    tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[s], k0, w.n0 + j * 64);
+                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[s], k0, w.n0 + j * 64,
+                                 bb);
                 else
-                    tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[s], w.n0 + j * 64, k0);
+                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[s], w.n0 + j * 64, k0,
+                                 bb);
             }
         }
     }
@@ -514,6 +559,23 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
         if ((int)i == withheld) continue;
         mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
     }
+}
+
+// The producer loop for the launch's operand layouts, chosen once: per-stage
+// branches in this single thread measurably slow the pipeline.
+template <int BN, bool B3>
+__device__ __forceinline__ void tc_produce_layout(const TcParams &p, const CUtensorMap *tmA,
+                                                  const CUtensorMap *tmB, uint8_t *sA,
+                                                  uint8_t *sB, uint64_t *full, uint64_t *empty,
+                                                  volatile int *abort_flag) {
+    if (!p.a_mn && !p.b_kmaj)
+        tc_producer<BN, false, false, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
+    else if (!p.a_mn)
+        tc_producer<BN, false, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
+    else if (!p.b_kmaj)
+        tc_producer<BN, true, false, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
+    else
+        tc_producer<BN, true, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
 }
 
 // Fused epilogue, first part: v[j] = act(alpha * v[j] + bias[gn + j]) for
@@ -566,7 +628,7 @@ __device__ __forceinline__ void apply_pre(const TcParams &p, int gn, float (&v)[
 // EPI: the fused bias / activation epilogue is compiled in (a separate
 // instantiation, so the plain kernel's epilogue code stays as small as it
 // can be: its size measurably affects the main loop's speed).
-template <int BN, bool EPI>
+template <int BN, bool EPI, bool B3>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
@@ -623,16 +685,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            // One loop per operand layout, chosen once: per-stage layout
-            // branches in this single thread measurably slow the pipeline.
-            if (!p.a_mn && !p.b_kmaj)
-                tc_producer<BN, false, false>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
-            else if (!p.a_mn)
-                tc_producer<BN, false, true>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
-            else if (!p.b_kmaj)
-                tc_producer<BN, true, false>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
-            else
-                tc_producer<BN, true, true>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
+            tc_produce_layout<BN, B3>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -718,6 +771,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
             const int gm = w.m_blk * TC_BM + row;
+            void *cmat = c_matrix(p, w.bidx);
             const int gn0 = w.n0;
             if (w.nparts == 1) {
 #pragma unroll 1
@@ -731,10 +785,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     if constexpr (EPI) apply_pre(p, gn0 + c * 32, v);
                     const float alpha = EPI ? 1.f : p.alpha;
                     if (p.c_tma)
-                        store_chunk_tma(p, alpha, &tmC, warp_stage, stage_seq, lane, gm - lane,
-                                        gn0 + c * 32, v);
+                        store_chunk_tma<B3>(p, alpha, cmat, w.bidx, &tmC, warp_stage, stage_seq, lane,
+                                        gm - lane, gn0 + c * 32, v);
                     else
-                        store_row_chunk(p, alpha, gm, gn0 + c * 32, v);
+                        store_row_chunk(p, alpha, cmat, gm, gn0 + c * 32, v);
                 }
                 tc_fence_before_sync();
                 mbar_arrive(&tempty[b]);
@@ -838,8 +892,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                 x.z = epi_pre(p.epi, p.alpha, x.z, min(n + 2, nl));
                                 x.w = epi_pre(p.epi, p.alpha, x.w, min(n + 3, nl));
                             }
-                            store_quad(p, EPI ? 1.f : p.alpha, w.m_blk * TC_BM + r, gn0 + 4 * c4,
-                                       x);
+                            store_quad(p, EPI ? 1.f : p.alpha, cmat, w.m_blk * TC_BM + r,
+                                       gn0 + 4 * c4, x);
                         }
                     }
                     if (et == 0) p.counters[tile] = 0u;  // ready for the next launch
@@ -896,7 +950,7 @@ struct Tc2Cfg {
 // one operand layout (as tc_producer).  Each CTA loads its own 128 rows of A
 // and its half of the tile's B columns; all copies complete on the even
 // CTA's full barrier.
-template <bool A_MN, bool B_KM>
+template <bool A_MN, bool B_KM, bool B3>
 __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMap *tmA,
                                              const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
                                              uint64_t *full, uint64_t *empty,
@@ -916,6 +970,7 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
         const uint32_t tx = 2u * (Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES);
         const int row0 = w.m_blk * 2 * TC_BM + (int)rank * TC_BM;
         const int col0 = w.n0 + (int)rank * half;
+        const int ab = w.bidx * p.a_bmul, bb = w.bidx * p.b_bmul;  // batch coordinates
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
             const int s = it % S;
             const uint32_t ph = (it / S) & 1u;
@@ -933,19 +988,19 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
             uint8_t *a_dst = sA + s * Cfg::A_BYTES;
             const int k0 = kb * TC_BK;
             if constexpr (A_MN) {
-                tma_load_2d_pair(a_dst, tmA, full_cl, row0, k0);
-                tma_load_2d_pair(a_dst + 8192, tmA, full_cl, row0 + 64, k0);
+                load_box_pair<B3>(a_dst, tmA, full_cl, row0, k0, ab);
+                load_box_pair<B3>(a_dst + 8192, tmA, full_cl, row0 + 64, k0, ab);
             } else {
-                tma_load_2d_pair(a_dst, tmA, full_cl, k0, row0);
+                load_box_pair<B3>(a_dst, tmA, full_cl, k0, row0, ab);
             }
             uint8_t *b_dst = sB + s * Cfg::B_BYTES;
             for (int j = 0; j < boxes; ++j) {
                 if constexpr (B_KM)
-                    tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, tmB, full_cl, k0,
-                                     col0 + j * 64);
+                    load_box_pair<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, full_cl, k0,
+                                      col0 + j * 64, bb);
                 else
-                    tma_load_2d_pair(b_dst + j * Cfg::B_BOX_BYTES, tmB, full_cl,
-                                     col0 + j * 64, k0);
+                    load_box_pair<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, full_cl,
+                                      col0 + j * 64, k0, bb);
             }
         }
     }
@@ -960,7 +1015,27 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
     }
 }
 
-template <bool EPI>
+template <bool B3>
+__device__ __forceinline__ void tc2_produce_layout(const TcParams &p, const CUtensorMap *tmA,
+                                                   const CUtensorMap *tmB, uint8_t *sA,
+                                                   uint8_t *sB, uint64_t *full, uint64_t *empty,
+                                                   volatile int *abort_flag, uint32_t rank,
+                                                   int pair, int npairs) {
+    if (!p.a_mn && !p.b_kmaj)
+        tc2_producer<false, false, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag, rank, pair,
+                                       npairs);
+    else if (!p.a_mn)
+        tc2_producer<false, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag, rank, pair,
+                                      npairs);
+    else if (!p.b_kmaj)
+        tc2_producer<true, false, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag, rank, pair,
+                                      npairs);
+    else
+        tc2_producer<true, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag, rank, pair,
+                                     npairs);
+}
+
+template <bool EPI, bool B3>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     bf16_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -1020,18 +1095,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            if (!p.a_mn && !p.b_kmaj)
-                tc2_producer<false, false>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank,
-                                           pair, npairs);
-            else if (!p.a_mn)
-                tc2_producer<false, true>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank,
-                                          pair, npairs);
-            else if (!p.b_kmaj)
-                tc2_producer<true, false>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank,
-                                          pair, npairs);
-            else
-                tc2_producer<true, true>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank,
-                                         pair, npairs);
+            tc2_produce_layout<B3>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank, pair,
+                                   npairs);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -1112,6 +1177,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tc_fence_after_sync();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
             const int gm = w.m_blk * 2 * TC_BM + (int)rank * TC_BM + row;
+            void *cmat = c_matrix(p, w.bidx);
 #pragma unroll 1
             for (int c = 0; c < w.width / 32; ++c) {
                 uint32_t r[32];
@@ -1123,10 +1189,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 if constexpr (EPI) apply_pre(p, w.n0 + c * 32, v);
                 const float alpha = EPI ? 1.f : p.alpha;
                 if (p.c_tma)
-                    store_chunk_tma(p, alpha, &tmC, warp_stage, stage_seq, lane, gm - lane,
-                                    w.n0 + c * 32, v);
+                    store_chunk_tma<B3>(p, alpha, cmat, w.bidx, &tmC, warp_stage, stage_seq, lane,
+                                    gm - lane, w.n0 + c * 32, v);
                 else
-                    store_row_chunk(p, alpha, gm, w.n0 + c * 32, v);
+                    store_row_chunk(p, alpha, cmat, gm, w.n0 + c * 32, v);
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -1164,17 +1230,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // per row, `outer` rows, `pitch` elements between rows; box of
 // box_inner x box_outer with 128-byte swizzle; out-of-range reads give 0.
 bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
-              uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {pitch * 2};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              uint64_t pitch, uint32_t box_inner, uint32_t box_outer, uint64_t depth,
+              uint64_t depth_stride) {
+    return encode_tensor_map_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, depth,
+                                pitch * 2, depth_stride * 2, box_inner, box_outer,
+                                CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Tensor maps of the A and B operands in the layouts p.a_mn / p.b_kmaj
@@ -1183,12 +1243,18 @@ bool make_map(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer
 // boxes, B stored N x K as 64 (K) x 64 (N) boxes.  Every box's x coordinate
 // is a multiple of 64 elements (128 bytes).
 bool make_ab_maps(CUtensorMap *ta, CUtensorMap *tb, const TcParams &p, const uint16_t *A,
-                  int64_t lda, const uint16_t *B, int64_t ldb) {
+                  int64_t lda, const uint16_t *B, int64_t ldb, const GemmOpts &o) {
     const uint64_t M = (uint64_t)p.M, N = (uint64_t)p.N, K = (uint64_t)p.K;
-    const bool ok_a = p.a_mn ? make_map(ta, A, M, K, (uint64_t)lda, 64, TC_BK)
-                             : make_map(ta, A, K, M, (uint64_t)lda, TC_BK, TC_BM);
-    const bool ok_b = p.b_kmaj ? make_map(tb, B, K, N, (uint64_t)ldb, TC_BK, 64)
-                               : make_map(tb, B, N, K, (uint64_t)ldb, 64, TC_BK);
+    // 2-D maps (depth 0) for one product; for a batch both are 3-D, an
+    // operand shared by the whole batch with depth 1.
+    const bool b3 = o.batch > 1;
+    const uint64_t da = b3 ? (p.a_bmul ? (uint64_t)o.batch : 1) : 0;
+    const uint64_t db = b3 ? (p.b_bmul ? (uint64_t)o.batch : 1) : 0;
+    const uint64_t sa = (uint64_t)o.stride_a, sb = (uint64_t)o.stride_b;
+    const bool ok_a = p.a_mn ? make_map(ta, A, M, K, (uint64_t)lda, 64, TC_BK, da, sa)
+                             : make_map(ta, A, K, M, (uint64_t)lda, TC_BK, TC_BM, da, sa);
+    const bool ok_b = p.b_kmaj ? make_map(tb, B, K, N, (uint64_t)ldb, TC_BK, 64, db, sb)
+                               : make_map(tb, B, N, K, (uint64_t)ldb, 64, TC_BK, db, sb);
     return ok_a && ok_b;
 }
 
@@ -1198,20 +1264,24 @@ bool make_ab_maps(CUtensorMap *ta, CUtensorMap *tb, const TcParams &p, const uin
 // 32 x 32, swizzled as store_chunk_tma lays out its staging buffers.  Also
 // decides p.c_tma: TMA stores need a 16-byte aligned C with a pitch that is
 // a multiple of 16 bytes; otherwise the epilogue stores directly.
-bool make_c_map(CUtensorMap *map, TcParams &p) {
+bool make_c_map(CUtensorMap *map, TcParams &p, int64_t batch) {
     const int esz = p.c_f32 ? 4 : 2;
-    p.c_tma = ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) && ((p.ldc * esz) % 16 == 0);
+    p.c_tma = ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) && ((p.ldc * esz) % 16 == 0) &&
+              ((p.c_bstride * esz) % 16 == 0);
     if (!p.c_tma) {
         memset(map, 0, sizeof(*map));
         return true;
     }
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.M};
-    cuuint64_t strides[1] = {(cuuint64_t)p.ldc * esz};
-    cuuint32_t box[2] = {32, 32};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, p.c_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    const uint64_t depth = batch > 1 ? (uint64_t)batch : 1;
+    const uint64_t dstride = (uint64_t)p.c_bstride * esz;
+    cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.M, depth};
+    cuuint64_t strides[2] = {(cuuint64_t)p.ldc * esz, dstride};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, p.c_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+              batch > 1 ? 3 : 2,
               p.C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               p.c_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -1220,27 +1290,31 @@ bool make_c_map(CUtensorMap *map, TcParams &p) {
 template <int BN>
 int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *ext,
               TcParams &p, const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
-              cudaStream_t stream) {
+              const GemmOpts &o, cudaStream_t stream) {
     using Cfg = TcCfg<BN>;
     static bool attr_done[kMaxDevices] = {};
     if (!attr_done[device]) {
-        if (cudaFuncSetAttribute(bf16_tc_kernel<BN, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::SMEM_ALLOC) != cudaSuccess ||
-            cudaFuncSetAttribute(bf16_tc_kernel<BN, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::SMEM_ALLOC) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+        const void *fns[4] = {(const void *)bf16_tc_kernel<BN, false, false>,
+                              (const void *)bf16_tc_kernel<BN, true, false>,
+                              (const void *)bf16_tc_kernel<BN, false, true>,
+                              (const void *)bf16_tc_kernel<BN, true, true>};
+        for (const void *fn : fns)
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::SMEM_ALLOC) != cudaSuccess)
+                return GEMM_ERR_CUDA;
         attr_done[device] = true;
     }
     alignas(64) CUtensorMap ta, tb, tc;
-    if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb)) return GEMM_ERR_CUDA;
-    if (!make_c_map(&tc, p)) return GEMM_ERR_CUDA;
+    if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb, o)) return GEMM_ERR_CUDA;
+    if (!make_c_map(&tc, p, o.batch)) return GEMM_ERR_CUDA;
 
     p.num_m_blk = (p.M + TC_BM - 1) / TC_BM;
     p.num_n_blk = (p.N + BN - 1) / BN;
     p.num_kb = (p.K + TC_BK - 1) / TC_BK;
-    const long long tiles = (long long)p.num_m_blk * p.num_n_blk;
+    const long long tiles_per_batch = (long long)p.num_m_blk * p.num_n_blk;
+    const long long tiles = tiles_per_batch * o.batch;  // over the whole batch
+    if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    p.tiles_per_batch = (int)tiles_per_batch;
     int splits = 1;
     const RuntimeConfig cfg = runtime_config();
     // Few tiles (at most half the SMs) and a long K: split K.  By default
@@ -1345,10 +1419,18 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
         }
     }
     const int grid = p.stream_k ? (int)sk_ctas : (int)(units < sm_count ? units : sm_count);
-    if (p.epi.on)
-        bf16_tc_kernel<BN, true><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, tc, p);
-    else
-        bf16_tc_kernel<BN, false><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(ta, tb, tc, p);
+    const int smem = Cfg::SMEM_ALLOC;
+    if (o.batch > 1) {
+        if (p.epi.on)
+            bf16_tc_kernel<BN, true, true><<<grid, TC_THREADS, smem, stream>>>(ta, tb, tc, p);
+        else
+            bf16_tc_kernel<BN, false, true><<<grid, TC_THREADS, smem, stream>>>(ta, tb, tc, p);
+    } else {
+        if (p.epi.on)
+            bf16_tc_kernel<BN, true, false><<<grid, TC_THREADS, smem, stream>>>(ta, tb, tc, p);
+        else
+            bf16_tc_kernel<BN, false, false><<<grid, TC_THREADS, smem, stream>>>(ta, tb, tc, p);
+    }
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -1369,31 +1451,33 @@ int max_resident_pairs(int device) {
     lc.attrs = attr;
     lc.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, bf16_tc2_kernel<false>, &lc) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, bf16_tc2_kernel<false, false>, &lc) != cudaSuccess ||
+        n <= 0)
         return 0;
     cache[device] = n;
     return n;
 }
 
 int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const uint16_t *B,
-               int64_t ldb, cudaStream_t stream) {
+               int64_t ldb, const GemmOpts &o, cudaStream_t stream) {
     using Cfg = Tc2Cfg;
     static bool attr_done[kMaxDevices] = {};
     if (!attr_done[device]) {
-        if (cudaFuncSetAttribute(bf16_tc2_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::SMEM_ALLOC) != cudaSuccess ||
-            cudaFuncSetAttribute(bf16_tc2_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::SMEM_ALLOC) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+        const void *fns[4] = {(const void *)bf16_tc2_kernel<false, false>,
+                              (const void *)bf16_tc2_kernel<true, false>,
+                              (const void *)bf16_tc2_kernel<false, true>,
+                              (const void *)bf16_tc2_kernel<true, true>};
+        for (const void *fn : fns)
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     Cfg::SMEM_ALLOC) != cudaSuccess)
+                return GEMM_ERR_CUDA;
         attr_done[device] = true;
     }
     const int pairs_max = max_resident_pairs(device);
     if (pairs_max <= 0) return GEMM_ERR_CUDA;
     alignas(64) CUtensorMap ta, tb, tc;
-    if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb)) return GEMM_ERR_CUDA;
-    if (!make_c_map(&tc, p)) return GEMM_ERR_CUDA;
+    if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb, o)) return GEMM_ERR_CUDA;
+    if (!make_c_map(&tc, p, o.batch)) return GEMM_ERR_CUDA;
     const RuntimeConfig cfg = runtime_config();
     p.num_m_blk = (p.M + 2 * TC_BM - 1) / (2 * TC_BM);  // 256-row pair tiles
     p.num_n_blk = (p.N + Cfg::BN - 1) / Cfg::BN;
@@ -1402,8 +1486,10 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     p.kb_per_split = p.num_kb;
     p.ws = nullptr;
     p.counters = nullptr;
-    const long long tiles = (long long)p.num_m_blk * p.num_n_blk;
+    const long long tiles_per_batch = (long long)p.num_m_blk * p.num_n_blk;
+    const long long tiles = tiles_per_batch * o.batch;  // over the whole batch
     if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    p.tiles_per_batch = (int)tiles_per_batch;
     // Raster band in 256-row blocks: 1024 rows when A and B fit in L2
     // together, else a band whose A panel takes about 32 MiB of L2.
     {
@@ -1443,8 +1529,13 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    const cudaError_t e = p.epi.on ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true>, ta, tb, tc, p)
-                                   : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false>, ta, tb, tc, p);
+    cudaError_t e;
+    if (o.batch > 1)
+        e = p.epi.on ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, true>, ta, tb, tc, p)
+                     : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, true>, ta, tb, tc, p);
+    else
+        e = p.epi.on ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, false>, ta, tb, tc, p)
+                     : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, false>, ta, tb, tc, p);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
@@ -1458,14 +1549,17 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
                   const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb, float beta,
                   void *C, int64_t ldc, bool c_f32, const GemmOpts *opts, cudaStream_t stream) {
     TcParams p{};
-    if (opts) {
-        p.a_mn = opts->trans_a ? 1 : 0;
-        p.b_kmaj = opts->trans_b ? 1 : 0;
-        p.epi.bias = opts->bias;
-        p.epi.bias_f32 = opts->bias_f32 ? 1 : 0;
-        p.epi.act = opts->act;
-        p.epi.on = (opts->bias != nullptr || opts->act != 0) ? 1 : 0;
-    }
+    GemmOpts o = opts ? *opts : GemmOpts{};
+    if (o.batch < 1) o.batch = 1;
+    p.a_mn = o.trans_a ? 1 : 0;
+    p.b_kmaj = o.trans_b ? 1 : 0;
+    p.epi.bias = o.bias;
+    p.epi.bias_f32 = o.bias_f32 ? 1 : 0;
+    p.epi.act = o.act;
+    p.epi.on = (o.bias != nullptr || o.act != 0) ? 1 : 0;
+    p.a_bmul = (o.batch > 1 && o.stride_a != 0) ? 1 : 0;
+    p.b_bmul = (o.batch > 1 && o.stride_b != 0) ? 1 : 0;
+    p.c_bstride = o.batch > 1 ? o.stride_c : 0;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -1475,7 +1569,8 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
     p.ldc = ldc;
     p.c_f32 = c_f32 ? 1 : 0;
     const int esz = c_f32 ? 4 : 2;
-    p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && ((ldc * esz) % 16 == 0);
+    p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && ((ldc * esz) % 16 == 0) &&
+              ((p.c_bstride * esz) % 16 == 0);
     p.fault_word = fault_word;
     const RuntimeConfig cfg = runtime_config();
     p.timeout_ns = (unsigned long long)cfg.watchdog_ms * 1000000ull;
@@ -1488,7 +1583,8 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
         // 128-wide tiles need half as many K slices for the same parallelism:
         // less partial-sum traffic and a shorter reduction (measured on the
         // 64 x 8192 x 8192 shape: 42 us vs 52 us).
-        const long long tiles256 = (long long)((M + TC_BM - 1) / TC_BM) * ((N + 255) / 256);
+        const long long tiles256 =
+            (long long)((M + TC_BM - 1) / TC_BM) * ((N + 255) / 256) * o.batch;
         if (bn == 256 && tiles256 * 2 <= sm_count && (K + TC_BK - 1) / TC_BK >= 8 &&
             cfg.split_k == 0)
             bn = 128;
@@ -1500,27 +1596,32 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
     if (cfg.cta_pair == 2) {
         pair = true;
     } else if (cfg.cta_pair == 0 && cfg.split_k == 0 && cfg.bf16_tile_n == 0 && M > TC_BM) {
-        const long long tiles1 = (long long)((M + TC_BM - 1) / TC_BM) * ((N + 255) / 256);
+        const long long tiles1 =
+            (long long)((M + TC_BM - 1) / TC_BM) * ((N + 255) / 256) * o.batch;
         const int num_kb = (K + TC_BK - 1) / TC_BK;
         pair = !(tiles1 * 2 <= sm_count && num_kb >= 8);
     }
-    if (pair) return launch_tc2(device, p, A, lda, B, ldb, stream);
-    return bn == 256 ? launch_tc<256>(device, sm_count, st, ext, p, A, lda, B, ldb, stream)
-                     : launch_tc<128>(device, sm_count, st, ext, p, A, lda, B, ldb, stream);
+    if (pair) return launch_tc2(device, p, A, lda, B, ldb, o, stream);
+    return bn == 256 ? launch_tc<256>(device, sm_count, st, ext, p, A, lda, B, ldb, o, stream)
+                     : launch_tc<128>(device, sm_count, st, ext, p, A, lda, B, ldb, o, stream);
 }
 
 }  // namespace
 
-bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
-                          uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
-                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+bool encode_tensor_map_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t inner, uint64_t outer, uint64_t depth, uint64_t pitch_bytes,
+                          uint64_t depth_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {pitch_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+    const cuuint32_t rank = depth == 0 ? 2 : 3;
+    if (depth == 1)  // any valid stride: the third coordinate is always 0
+        depth_stride_bytes = (pitch_bytes * (outer > 0 ? outer : 1) + 15) / 16 * 16;
+    cuuint64_t dims[3] = {inner, outer, depth};
+    cuuint64_t strides[2] = {pitch_bytes, depth_stride_bytes};
+    cuuint32_t box[3] = {box_inner, box_outer, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

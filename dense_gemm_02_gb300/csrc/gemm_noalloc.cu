@@ -87,7 +87,7 @@ extern "C" int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
     if ((rc = scratch_for_current_device(&device, &slot)) != GEMM_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (alpha == 0.f || K == 0)
-        return launch_scale_c((int)M, (int)N, beta, C, ldc, c_f32, s) == cudaSuccess
+        return launch_scale_c((int)M, (int)N, beta, C, ldc, c_f32, 1, 0, s) == cudaSuccess
                    ? GEMM_OK
                    : GEMM_ERR_CUDA;
     const bool tma_ok = ((reinterpret_cast<uintptr_t>(A) & 15) == 0) &&

@@ -89,25 +89,40 @@ __host__ __device__ __forceinline__ void grouped_tile_coords(int tile, int num_m
     n_blk = r / gm;
 }
 
-// Encodes a 2-D tiled tensor map (cuTensorMapEncodeTiled through the
-// runtime's driver entry point): `inner` contiguous elements per row,
-// `outer` rows, `pitch_bytes` between rows, boxes of box_inner x box_outer.
-// Out-of-range reads return zero.  False if the driver call failed.
-bool encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
-                          uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
-                          uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+// Encodes a 3-D tiled tensor map (cuTensorMapEncodeTiled through the
+// runtime's driver entry point) over `depth` matrices depth_stride_bytes
+// apart, each `outer` rows of `inner` contiguous elements, `pitch_bytes`
+// between rows; boxes of box_inner x box_outer x 1.  depth <= 1 is one
+// matrix (the stride is then ignored).  Out-of-range reads return zero.
+// False if the driver call failed.
+bool encode_tensor_map_3d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base,
+                          uint64_t inner, uint64_t outer, uint64_t depth, uint64_t pitch_bytes,
+                          uint64_t depth_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle);
+
+// Whether a strided batch can be fetched by 3-D TMA: one matrix, or a batch
+// stride (bytes) that is 0 (shared matrix) or a multiple of 16 no smaller
+// than one matrix's span.
+inline bool tma_batch_stride_ok(int64_t batch, int64_t stride_bytes, int64_t span_bytes) {
+    return batch <= 1 || stride_bytes == 0 ||
+           (stride_bytes % 16 == 0 && stride_bytes >= span_bytes);
+}
 
 // ---- kernel launchers (return cudaSuccess or the launch error) ----
 
-// Operand layouts and fused epilogue of the *_ex entry points (host side):
-// trans_a: A stored K x M; trans_b: B stored N x K; bias: nullptr or N
-// values (fp32 when bias_f32, else bf16); act: a gemm_act_t.  A null
-// GemmOpts pointer means row-major operands and the plain epilogue.
+// Operand layouts, fused epilogue and strided batch of the extended entry
+// points (host side): trans_a: A stored K x M; trans_b: B stored N x K;
+// bias: nullptr or N values (fp32 when bias_f32, else bf16); act: a
+// gemm_act_t; batch matrices, matrix i at A + i * stride_a (elements; 0
+// shares one matrix among all), likewise B and C.  A null GemmOpts pointer
+// means one row-major product with the plain epilogue.
 struct GemmOpts {
-    int trans_a, trans_b;
-    const void *bias;
-    int bias_f32;
-    int act;
+    int trans_a = 0, trans_b = 0;
+    const void *bias = nullptr;
+    int bias_f32 = 0;
+    int act = 0;
+    int64_t batch = 1;
+    int64_t stride_a = 0, stride_b = 0, stride_c = 0;
 };
 
 cudaError_t launch_sgemm_simt(int M, int N, int K, float alpha, const float *A, int64_t lda,
@@ -128,9 +143,10 @@ cudaError_t launch_gemm_simt_generic(int M, int N, int K, float alpha, const voi
                                      void *C, int64_t ldc, bool bf16_in, bool c_f32,
                                      const GemmOpts *opts, cudaStream_t stream);
 
-// C = beta * C (C = 0 without reading it when beta == 0).
+// C = beta * C (C = 0 without reading it when beta == 0), for `batch`
+// matrices stride_c elements apart.
 cudaError_t launch_scale_c(int M, int N, float beta, void *C, int64_t ldc, bool c_f32,
-                           cudaStream_t stream);
+                           int64_t batch, int64_t stride_c, cudaStream_t stream);
 
 // Host-side argument checks shared by the entry points.  Returns GEMM_OK,
 // an error, or 1 for "valid, nothing to do" (M == 0 or N == 0).

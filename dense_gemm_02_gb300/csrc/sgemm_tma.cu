@@ -61,6 +61,11 @@ struct TmaParams {
     // Partial-wave K split: blocks past tiles_main take one K slice
     // (kt_per_split 32-deep steps) of a tile split `splits` ways.
     int tiles_main, splits, kt_per_split;
+    // Strided batch: tile t of the launch is tile t % tiles_per_batch of
+    // matrix t / tiles_per_batch; a_bmul / b_bmul are 0 for a matrix shared
+    // by the whole batch; C matrix i starts c_bstride elements after C.
+    int tiles_per_batch, a_bmul, b_bmul;
+    long long c_bstride;
     float *ws;           // fp32 partial tiles of the split tiles
     unsigned *counters;  // one per split tile
 };
@@ -87,9 +92,12 @@ __global__ void __launch_bounds__(TTHREADS, 2)
         tile = p.tiles_main + v / p.splits;
         slice = v - (v / p.splits) * p.splits;
     }
+    const int bidx = tile / p.tiles_per_batch;
     int m_blk, n_blk;
-    grouped_tile_coords(tile, p.num_m_blk, p.num_n_blk, kRasterGroup, m_blk, n_blk);
+    grouped_tile_coords(tile - bidx * p.tiles_per_batch, p.num_m_blk, p.num_n_blk, kRasterGroup,
+                        m_blk, n_blk);
     const int m0 = m_blk * TBM, n0 = n_blk * TBN;
+    const int ab = bidx * p.a_bmul, bb = bidx * p.b_bmul;  // TMA batch coordinates
     const int KT_all = (p.K + TBK - 1) / TBK;
     const int kt0 = slice < 0 ? 0 : slice * p.kt_per_split;
     const int KT = slice < 0 ? KT_all : min(p.kt_per_split, KT_all - kt0);  // >= 1
@@ -107,8 +115,8 @@ __global__ void __launch_bounds__(TTHREADS, 2)
         const int s = kt % TSTAGES;
         uint8_t *st = smem + s * TSTAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], TSTAGE_BYTES);
-        tma_load_2d(st, &tmA, &full[s], (kt0 + kt) * TBK, m0);
-        tma_load_2d(st + TA_BYTES, &tmB, &full[s], n0, (kt0 + kt) * TBK);
+        tma_load_3d(st, &tmA, &full[s], (kt0 + kt) * TBK, m0, ab);
+        tma_load_3d(st + TA_BYTES, &tmB, &full[s], n0, (kt0 + kt) * TBK, bb);
     };
     int issued = 0;
     if (tid == 0)
@@ -239,7 +247,7 @@ __global__ void __launch_bounds__(TTHREADS, 2)
     for (int i = 0; i < 8; ++i) {
         const int row = m0 + wm * 64 + tm + 8 * i;
         if (row >= p.M) continue;
-        float *crow = p.C + (long long)row * p.ldc;
+        float *crow = p.C + bidx * p.c_bstride + (long long)row * p.ldc;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int col = n0 + wn * 32 + tn * 4 + 16 * h;
@@ -284,19 +292,24 @@ int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const fl
             return GEMM_ERR_CUDA;
         attr_done[st->device] = true;
     }
+    const GemmOpts o = opts ? *opts : GemmOpts{};
+    const int64_t batch = o.batch > 1 ? o.batch : 1;
     alignas(64) CUtensorMap ta, tb;
-    if (!encode_tensor_map_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, (uint64_t)K, (uint64_t)M,
-                              (uint64_t)lda * 4, TBK, TBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, (uint64_t)N, (uint64_t)K,
-                              (uint64_t)ldb * 4, TBN, TBK, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_tensor_map_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, (uint64_t)K, (uint64_t)M,
+                              o.stride_a ? (uint64_t)batch : 1, (uint64_t)lda * 4,
+                              (uint64_t)o.stride_a * 4, TBK, TBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tensor_map_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, B, (uint64_t)N, (uint64_t)K,
+                              o.stride_b ? (uint64_t)batch : 1, (uint64_t)ldb * 4,
+                              (uint64_t)o.stride_b * 4, TBN, TBK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return GEMM_ERR_CUDA;
     TmaParams p{};
-    if (opts) {
-        p.epi.bias = opts->bias;
-        p.epi.bias_f32 = opts->bias_f32 ? 1 : 0;
-        p.epi.act = opts->act;
-        p.epi.on = (opts->bias != nullptr || opts->act != 0) ? 1 : 0;
-    }
+    p.epi.bias = o.bias;
+    p.epi.bias_f32 = o.bias_f32 ? 1 : 0;
+    p.epi.act = o.act;
+    p.epi.on = (o.bias != nullptr || o.act != 0) ? 1 : 0;
+    p.a_bmul = o.stride_a && batch > 1 ? 1 : 0;
+    p.b_bmul = o.stride_b && batch > 1 ? 1 : 0;
+    p.c_bstride = batch > 1 ? o.stride_c : 0;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -304,13 +317,16 @@ int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const fl
     p.beta = beta;
     p.C = C;
     p.ldc = ldc;
-    p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && (ldc % 4 == 0);
+    p.c_vec = ((reinterpret_cast<uintptr_t>(C) & 15) == 0) && (ldc % 4 == 0) &&
+              (p.c_bstride % 4 == 0);
     p.num_m_blk = (M + TBM - 1) / TBM;
     p.num_n_blk = (N + TBN - 1) / TBN;
     p.fault_word = st->fault_word;
     p.timeout_ns = (unsigned long long)runtime_config().watchdog_ms * 1000000ull;
-    const long long tiles = (long long)p.num_m_blk * p.num_n_blk;
+    const long long tiles_per_batch = (long long)p.num_m_blk * p.num_n_blk;
+    const long long tiles = tiles_per_batch * batch;
     if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    p.tiles_per_batch = (int)tiles_per_batch;
 
     // Partial last wave.  The kernel is bound by the FP32 pipe, so an SM
     // finishes its tiles at about the same rate whether one or two CTAs

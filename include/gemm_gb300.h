@@ -170,6 +170,35 @@ GEMM_API int gemm_f32_ex(int64_t M, int64_t N, int64_t K, float alpha,
                          void *stream);
 
 /*
+ * Strided batched GEMMs: for i = 0 .. batch-1,
+ *     C_i = act(alpha * op(A_i) * op(B_i) + bias) + beta * C_i
+ * with A_i = A + i * stride_a, B_i = B + i * stride_b, C_i = C + i * stride_c
+ * (strides in elements).  "Blackwell BF16 GEMM ..." (lshu.cn), section 3.1,
+ * lists grouped / batched GEMM among the cuBLASLt capabilities a GEMM
+ * library covers; this is the strided form of BLAS.  Every matrix has the
+ * same M, N, K, pitches, layouts (opts) and bias.
+ *   batch      >= 0 (0: nothing is done)
+ *   stride_a   >= 0; 0 shares one A among all products (likewise stride_b)
+ *   stride_c   C matrices must not overlap: stride_c * element size at least
+ *              the span of one C (else GEMM_ERR_ALIAS)
+ * The whole batch runs as one launch; the tensor-core and TMA kernels take
+ * it when pitches and nonzero batch strides are multiples of 16 bytes and a
+ * nonzero stride is at least one matrix's span, otherwise the generic
+ * kernel.  C must not overlap any A, B or bias byte the batch reads
+ * (GEMM_ERR_ALIAS); negative strides are GEMM_ERR_INVALID_ARG.  Otherwise
+ * the rules of gemm_bf16_ex / gemm_f32_ex.
+ */
+GEMM_API int gemm_bf16_batched(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha,
+                               const uint16_t *A, int64_t lda, int64_t stride_a,
+                               const uint16_t *B, int64_t ldb, int64_t stride_b, float beta,
+                               void *C, int64_t ldc, int64_t stride_c, int c_type,
+                               const gemm_opts_t *opts, void *stream);
+GEMM_API int gemm_f32_batched(int64_t batch, int64_t M, int64_t N, int64_t K, float alpha,
+                              const float *A, int64_t lda, int64_t stride_a, const float *B,
+                              int64_t ldb, int64_t stride_b, float beta, float *C, int64_t ldc,
+                              int64_t stride_c, const gemm_opts_t *opts, void *stream);
+
+/*
  * Allocation-free BF16 GEMM.  The source pages have no counterpart: this is
  * an interface for callers that cannot call cudaMalloc at all, for example
  * code that runs inside a host whose device memory is fully owned by its own

@@ -157,7 +157,11 @@ def _vector(x, name):
 
 def gemm_fused(A, B, C=None, alpha=1.0, beta=0.0, bias=None, act=ACT_NONE, threads=None,
                M=None, N=None, K=None):
-    """act(alpha * A @ B + bias) + beta * C in double (A, B logical, row-major)."""
+    """act(alpha * A @ B + bias) + beta * C in double (A, B logical, row-major).
+    Without bias and activation this is the plain gemm (alpha == 0 then gives
+    beta * C itself, as there)."""
+    if bias is None and int(act) == ACT_NONE:
+        return gemm(A, B, C, alpha=alpha, beta=beta, threads=threads, M=M, N=N, K=K)
     lib = _load()
     R = gemm(A, B, None, alpha=alpha, beta=0.0, threads=threads, M=M, N=N, K=K)
     tb, pb, _kb = _vector(bias, "bias")

@@ -22,7 +22,7 @@
  * Readings where the pages are silent (the BLAS conventions):
  *  - beta == 0: C is not read (it may hold NaN); the result is alpha*A*B.
  *  - alpha == 0 or K == 0: A and B are not read; the result is beta*C
- *    (zero when beta == 0).
+ *    itself, -0 included (+0 when beta == 0).
  *  - Inputs are widened exactly to double (fp32 and bf16 are subsets of
  *    double) and every product of two widened fp32/bf16 values is exact in
  *    double; only the running sums round.  The sum runs over k in
@@ -77,8 +77,12 @@ static void *gemm_rows(void *arg) {
             }
         }
         for (int64_t j = 0; j < g->N; ++j) {
-            double r = (g->alpha != 0.0) ? g->alpha * acc[j] : 0.0;
-            if (g->beta != 0.0) r += g->beta * load_elem(g->c_type, g->C, i * g->ldc + j);
+            const double bc =
+                (g->beta != 0.0) ? g->beta * load_elem(g->c_type, g->C, i * g->ldc + j) : 0.0;
+            /* alpha == 0: the result is beta*C itself (its sign of zero too);
+             * beta == 0: alpha*A*B itself */
+            const double ab = g->alpha * acc[j];
+            const double r = (g->alpha == 0.0) ? bc : (g->beta != 0.0) ? ab + bc : ab;
             g->R[i * g->ldr + j] = r;
         }
     }
@@ -154,8 +158,8 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, double alpha,
         if (alpha != 0.0)
             for (int64_t k = 0; k < K; ++k)
                 sum += load_elem(a_type, A, i * lda + k) * load_elem(b_type, B, k * ldb + j);
-        double r = (alpha != 0.0) ? alpha * sum : 0.0;
-        if (beta != 0.0) r += beta * load_elem(c_type, C, i * ldc + j);
+        const double bc = (beta != 0.0) ? beta * load_elem(c_type, C, i * ldc + j) : 0.0;
+        const double r = (alpha == 0.0) ? bc : (beta != 0.0) ? alpha * sum + bc : alpha * sum;
         out[e] = r;
     }
     return 0;

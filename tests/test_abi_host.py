@@ -126,6 +126,29 @@ def test_extended_entry_point_errors(lib):
         assert f(0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, *extra, ta, None) == b.GEMM_OK
 
 
+def test_batched_entry_point_errors(lib):
+    """gemm_bf16_batched / gemm_f32_batched: batch and stride checks run
+    before any CUDA call."""
+    from dense_gemm_02_gb300 import binding as b
+
+    fake = 1 << 20
+    for f, extra in ((b.gemm_bf16_batched, (b.GEMM_OUT_F32,)), (b.gemm_f32_batched, ())):
+        def call(batch, sa, sb, sc, A=fake, B=fake + (1 << 16), C=fake + (1 << 18), opts=None):
+            return f(batch, 4, 4, 4, 1.0, A, 4, sa, B, 4, sb, 0.0, C, 4, sc, *extra, opts, None)
+
+        assert call(-1, 16, 16, 16) == b.GEMM_ERR_INVALID_ARG
+        assert call(0, 16, 16, 16, A=None, B=None, C=None) == b.GEMM_OK  # empty batch
+        assert call(2, -16, 16, 16) == b.GEMM_ERR_INVALID_ARG
+        assert call(2, 16, 16, -16) == b.GEMM_ERR_INVALID_ARG
+        # C matrices 8 elements apart overlap (one 4 x 4 C spans 16)
+        assert call(2, 16, 16, 8) == b.GEMM_ERR_ALIAS
+        assert call(3, 16, 16, 0) == b.GEMM_ERR_ALIAS
+        # the third C lands on B's first matrix
+        assert call(3, 0, 0, 1 << 14, C=fake + (1 << 16) - 2 * (1 << 14) * 4) == b.GEMM_ERR_ALIAS
+        # unknown option still reported first
+        assert call(2, 16, 16, 16, opts=b.make_opts(act=9)) == b.GEMM_ERR_INVALID_ARG
+
+
 def test_config_keys(lib):
     from dense_gemm_02_gb300 import binding as b
 

@@ -112,6 +112,30 @@ def test_alpha_beta_conventions(oracle):
     assert np.array_equal(oracle.gemm(A, B, C, alpha=0.5, beta=1.0), expect_half)
 
 
+def test_alpha_zero_result_is_beta_c_including_its_sign_of_zero(oracle):
+    # BLAS reading: alpha == 0 (or K == 0) gives beta*C itself, so a zero
+    # of C scaled by a negative beta is -0; beta == 0 gives alpha*A*B itself,
+    # so an exact zero product scaled by a negative alpha is -0.
+    M, K, N = 3, 4, 2
+    C = np.zeros((M, N), np.float32)
+    R = oracle.gemm(np.ones((M, K), np.float32), np.ones((K, N), np.float32), C,
+                    alpha=0.0, beta=-2.0)
+    assert np.signbit(R).all() and (R == 0).all()
+    R0 = oracle.gemm(np.zeros((M, 0), np.float32), np.zeros((0, N), np.float32), C,
+                     alpha=1.0, beta=-2.0)
+    assert np.signbit(R0).all()
+    Z = oracle.gemm(np.zeros((M, K), np.float32), np.ones((K, N), np.float32), None,
+                    alpha=-1.0, beta=0.0)
+    assert np.signbit(Z).all() and (Z == 0).all()
+    # both terms present: IEEE sum of (-0) + (+0) is +0
+    P = oracle.gemm(np.zeros((M, K), np.float32), np.ones((K, N), np.float32), C,
+                    alpha=-1.0, beta=1.0)
+    assert not np.signbit(P).any()
+    E = oracle.gemm_entries(np.zeros((M, K), np.float32), np.ones((K, N), np.float32),
+                            np.array([0, 2]), np.array([1, 0]), C=C, alpha=0.0, beta=-3.0)
+    assert np.signbit(E).all()
+
+
 def _exact_product(A, B, C, alpha, beta):
     """Independent exact evaluation with Fractions, column-major loop order."""
     M, K = len(A), len(A[0]) if A else 0
