@@ -65,6 +65,11 @@ def parse_args():
                          "comma-separated: a layout nn|tn|nt|tt (t: that operand stored "
                          "transposed), 'bias' (N fp32 values), an activation relu|gelu; "
                          "'plain' = the plain entry points")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="run each workload as a strided batch of this many products "
+                         "(gemm_batched, one launch)")
+    ap.add_argument("--shape", default=None, metavar="MxNxK",
+                    help="override the workload's M, N, K (same distributions)")
     ap.add_argument("--config", action="append", default=[], metavar="KEY=VALUE",
                     help="library tuning knob (gemm_set_config), may repeat")
     return ap.parse_args()
@@ -291,6 +296,7 @@ def config_block(workloads, args):
                       "kernel events exclude host launch overhead",
         "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU",
         "variant": getattr(args, "variant", "plain"),
+        "batch": getattr(args, "batch", 1),
         "library_config": list(getattr(args, "config", [])),
     }
 
@@ -352,11 +358,20 @@ def run_ours(args, dist):
     for kv in args.config:
         key, val = kv.split("=", 1)
         g.set_config(key, int(val))
+    import dataclasses
+
+    import numpy as np
+
     import gemm_inputs as gi
 
     workloads = workloads_for(args.workload)
+    if args.shape:
+        M, N, K = (int(x) for x in args.shape.lower().split("x"))
+        workloads = [dataclasses.replace(w, M=M, N=N, K=K, name=f"{w.name}@{M}x{N}x{K}")
+                     for w in workloads]
+    nb = max(1, args.batch)
     v_ta, v_tb, v_bias, v_act = parse_variant(args.variant)
-    extended = args.variant != "plain"
+    extended = args.variant != "plain" or nb > 1
     if extended:
         args.no_e2e = True  # the host-buffer API runs the plain entry points
     peaks, peak_src = load_peaks()
@@ -368,6 +383,11 @@ def run_ours(args, dist):
     host_ops = []
     for w in workloads:
         A, B, C = w.operands()
+        if nb > 1:  # matrices 0..nb-1 of a strided batch, stacked
+            ops = [w.batch_operands(i) for i in range(nb)]
+            A = np.stack([o[0] for o in ops])
+            B = np.stack([o[1] for o in ops])
+            C = np.stack([o[2] for o in ops]) if ops[0][2] is not None else None
         if w.dtype == "f32":
             hA, hB = torch.from_numpy(A), torch.from_numpy(B)
         else:
@@ -383,11 +403,11 @@ def run_ours(args, dist):
         # Transposed storage: the same logical operand, held K x M (or N x
         # K) row-major; the library reads that layout in place.
         if v_ta:
-            dA = dA.t().contiguous().t()
+            dA = dA.transpose(-1, -2).contiguous().transpose(-1, -2)
         if v_tb:
-            dB = dB.t().contiguous().t()
-        dC = hC.cuda() if hC is not None else torch.empty((w.M, w.N), dtype=out_dt,
-                                                            device="cuda")
+            dB = dB.transpose(-1, -2).contiguous().transpose(-1, -2)
+        cshape = (nb, w.M, w.N) if nb > 1 else (w.M, w.N)
+        dC = hC.cuda() if hC is not None else torch.empty(cshape, dtype=out_dt, device="cuda")
         bias = (torch.from_numpy(gi.draw("normal", 0xB1A5 + w.index, 3, (w.N,))).cuda()
                 if v_bias else None)
         dev_ops.append((w, dA, dB, dC, bias))
@@ -397,7 +417,9 @@ def run_ours(args, dist):
     stream = torch.cuda.current_stream()
 
     def launch(w, dA, dB, dC, bias):
-        if extended:
+        if nb > 1:
+            g.gemm_batched(dA, dB, dC, alpha=w.alpha, beta=w.beta, bias=bias, act=v_act)
+        elif extended:
             g.gemm_ex(dA, dB, dC, alpha=w.alpha, beta=w.beta, bias=bias, act=v_act)
         elif w.dtype == "f32":
             g.sgemm(dA, dB, dC, alpha=w.alpha, beta=w.beta)
@@ -436,7 +458,7 @@ def run_ours(args, dist):
     per_kernel_ms = [[ev[i].elapsed_time(ev[i + 1]) for ev in events] for i in range(nk)]
     step_ms = [sum(per_kernel_ms[i][s] for i in range(nk)) for s in range(args.steps)]
     total_s = dist.max(sum(step_ms) / 1e3)
-    flops_step = sum(w.flops for w in workloads)
+    flops_step = sum(w.flops for w in workloads) * nb
     value = dist.sum(flops_step * args.steps) / total_s / 1e12
     gpu_launches = nk * args.steps
 
@@ -447,10 +469,10 @@ def run_ours(args, dist):
     rooflines = {}
     for i, w in enumerate(workloads):
         ms = statistics.mean(per_kernel_ms[i])
-        tflops = w.flops / (ms / 1e3) / 1e12
-        gbs = w.min_bytes() / (ms / 1e3) / 1e9
+        tflops = w.flops * nb / (ms / 1e3) / 1e12
+        gbs = w.min_bytes() * nb / (ms / 1e3) / 1e9
         entry = {"ms_mean": ms, "ms_median": statistics.median(per_kernel_ms[i]),
-                 "ms_min": min(per_kernel_ms[i]), "tflops": tflops, "min_bytes": w.min_bytes(),
+                 "ms_min": min(per_kernel_ms[i]), "tflops": tflops, "min_bytes": w.min_bytes() * nb,
                  "achieved_gbs_min_bytes": gbs}
         if w.dtype == "f32":
             rl = {"bound": "alu", "achieved": tflops, "peak": fp32_peak, "unit": "TFLOP/s",

@@ -64,6 +64,23 @@ class Workload:
             C = _draw_rows(kind_c, seed, 2, self.M, self.N, self.sigma_c, self.out, rows)
         return A, B, C
 
+    def batch_operands(self, i: int, integer: bool = False):
+        """(A, B, C_in) of matrix i of a strided batch of this shape: the
+        elements after those of matrices 0..i-1 on the same streams (matrix
+        0 is ``operands()``)."""
+        seed = self.seed + (INTEGER_PASS_OFFSET if integer else 0)
+        kind_a = "integer" if integer else self.dist
+        A = draw(kind_a, seed, 0, (self.M, self.K), sigma=self.sigma_a, dtype=self.dtype,
+                 offset=i * self.M * self.K)
+        B = draw(kind_a, seed, 1, (self.K, self.N), sigma=self.sigma_b, dtype=self.dtype,
+                 offset=i * self.K * self.N)
+        C = None
+        if self.beta != 0:
+            kind_c = "integer" if integer else self.c_dist
+            C = draw(kind_c, seed, 2, (self.M, self.N), sigma=self.sigma_c, dtype=self.out,
+                     offset=i * self.M * self.N)
+        return A, B, C
+
 
 def _draw_rows(kind, seed, stream, rows_total, cols, sigma, dtype, rows):
     if rows is None:

@@ -59,3 +59,20 @@ def test_bf16_operand_rounding_matches_torch():
     assert np.array_equal(ours, ref)
     back = gi.bf16_bits_to_f32(ours)
     assert np.array_equal(back, torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+
+
+def test_batch_operands_continue_the_streams():
+    from gemm_inputs.workloads import WORKLOADS
+
+    w = WORKLOADS["bf16_mlp_8192x14336x4096"]
+    import dataclasses
+
+    small = dataclasses.replace(w, M=6, N=5, K=4)
+    A0, B0, C0 = small.operands()
+    a0, b0, c0 = small.batch_operands(0)
+    assert np.array_equal(A0, a0) and np.array_equal(B0, b0) and np.array_equal(C0, c0)
+    a1, b1, c1 = small.batch_operands(1)
+    # matrix 1 holds the next elements of each stream
+    big_a = gi.draw(small.dist, small.seed, 0, (12, 4), sigma=small.sigma_a, dtype=small.dtype)
+    assert np.array_equal(big_a[6:], a1)
+    assert not np.array_equal(b0, b1) and not np.array_equal(c0, c1)
