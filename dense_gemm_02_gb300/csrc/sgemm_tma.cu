@@ -137,7 +137,9 @@ __global__ void __launch_bounds__(TTHREADS, 2)
     bool failed = false;
 #pragma unroll 1
     for (; kt < KT; ++kt) {
-        const bool ok = mbar_wait(&full[s], ph, never, p.timeout_ns);
+        // Plain polling here: all 256 threads wait on the stage, and a
+        // suspend hint measured 1% slower for this kernel.
+        const bool ok = mbar_wait(&full[s], ph, never, p.timeout_ns, false, 0);
         if (__syncthreads_or(!ok)) {
             failed = true;
             break;
