@@ -578,6 +578,21 @@ __device__ __forceinline__ void tc_produce_layout(const TcParams &p, const CUten
         tc_producer<BN, true, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
 }
 
+// Loads two consecutive 32-column chunks (64 floats) of this thread's row
+// of a partial tile from the split-K workspace (float4 i of the pair at
+// src + i * 32: the warp-coalesced workspace layout), all sixteen loads
+// issued together.
+__device__ __forceinline__ void load_partial_chunks(const float4 *src, float (&x)[2][32]) {
+    float4 t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = __ldcg(src + i * 32);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float *d = &x[i >> 3][(i & 7) * 4];
+        d[0] = t[i].x, d[1] = t[i].y, d[2] = t[i].z, d[3] = t[i].w;
+    }
+}
+
 // Fused epilogue, first part: v[j] = act(alpha * v[j] + bias[gn + j]) for
 // the 32 columns gn..gn+31 (columns past N use bias[N - 1]; they are never
 // stored).  The store helpers then add beta * C with alpha = 1.  The bias
@@ -793,20 +808,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tc_fence_before_sync();
                 mbar_arrive(&tempty[b]);
             } else {
-                float *wrow = p.ws + (((size_t)tile * p.max_parts + w.part) * TC_BM + row) * BN;
+                // Split tile: this slice's fp32 partial goes to the workspace
+                // in a warp-coalesced layout (per slice: float4
+                // ((q * BN/32 + chunk) * 8 + j) * 32 + lane holds columns
+                // chunk * 32 + 4j .. +3 of row q * 32 + lane); warps whose 32
+                // rows all lie past M skip it.
+                const bool rows_in = w.m_blk * TC_BM + q * 32 < p.M;
+                const size_t slice4 = (size_t)TC_BM * BN / 4;
+                float4 *wq = reinterpret_cast<float4 *>(p.ws) +
+                             ((size_t)tile * p.max_parts + w.part) * slice4 +
+                             (size_t)q * (BN / 32) * 8 * 32 + lane;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tbase + c * 32, r);
                     tmem_ld_wait();
-                    if (gm < p.M) {
-                        float4 *dst = reinterpret_cast<float4 *>(wrow + c * 32);
+                    if (rows_in) {
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            __stcg(dst + j, make_float4(__uint_as_float(r[4 * j]),
-                                                        __uint_as_float(r[4 * j + 1]),
-                                                        __uint_as_float(r[4 * j + 2]),
-                                                        __uint_as_float(r[4 * j + 3])));
+                            __stcg(wq + (c * 8 + j) * 32,
+                                   make_float4(__uint_as_float(r[4 * j]),
+                                               __uint_as_float(r[4 * j + 1]),
+                                               __uint_as_float(r[4 * j + 2]),
+                                               __uint_as_float(r[4 * j + 3])));
                     }
                 }
                 tc_fence_before_sync();
@@ -818,84 +842,42 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     *last_flag = (old == (unsigned)(w.nparts - 1)) ? 1 : 0;
                 }
                 named_bar_sync(TC_EPI_BAR, TC_EPI_THREADS);
-                if (*last_flag) {
-                    // Last slice of this tile: all epilogue threads sum the
-                    // slices, each element over slices 0..S-1 in order, with
-                    // coalesced 16-byte loads (four columns per element).
+                if (*last_flag && rows_in) {
+                    // Last slice of this tile: each thread sums its own row
+                    // over slices 0..S-1 in order, two 32-column chunks at a
+                    // time with a slice's sixteen loads in flight together,
+                    // then stores the chunks as the plain epilogue does.
                     __threadfence();
-                    const int rows = min(TC_BM, p.M - w.m_blk * TC_BM);
-                    const int c4n = BN / 4;
-                    const float *base = p.ws + (size_t)tile * p.max_parts * TC_BM * BN;
-                    const size_t slice = (size_t)TC_BM * BN;
-                    // Four elements per thread per pass and up to four slices
-                    // per step keep 16 independent loads in flight.
-                    const int total = rows * c4n;
-                    const float4 *b4 = reinterpret_cast<const float4 *>(base);
-                    const size_t slice4 = slice / 4;
+                    const float4 *rq = reinterpret_cast<const float4 *>(p.ws) +
+                                       (size_t)tile * p.max_parts * slice4 +
+                                       (size_t)q * (BN / 32) * 8 * 32 + lane;
 #pragma unroll 1
-                    for (int e0 = et; e0 < total; e0 += 4 * TC_EPI_THREADS) {
-                        float4 v[4];
-                        int off[4];
-                        bool in[4];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int e = e0 + q * TC_EPI_THREADS;
-                            in[q] = e < total;
-                            const int r = e / c4n, c4 = e - r * c4n;
-                            off[q] = r * (BN / 4) + c4;
-                            v[q] = in[q] ? __ldcg(b4 + off[q]) : make_float4(0.f, 0.f, 0.f, 0.f);
-                        }
-                        int sl = 1;
+                    for (int c = 0; c < BN / 32; c += 2) {
+                        float v[2][32];
+                        load_partial_chunks(rq + c * 8 * 32, v);
 #pragma unroll 1
-                        for (; sl + 3 < w.nparts; sl += 4) {
-                            float4 x[4][4];
+                        for (int sl = 1; sl < w.nparts; ++sl) {
+                            float x[2][32];
+                            load_partial_chunks(rq + sl * slice4 + c * 8 * 32, x);
 #pragma unroll
-                            for (int t = 0; t < 4; ++t)
+                            for (int h = 0; h < 2; ++h)
 #pragma unroll
-                                for (int q = 0; q < 4; ++q)
-                                    x[t][q] = in[q] ? __ldcg(b4 + (sl + t) * slice4 + off[q])
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                            for (int t = 0; t < 4; ++t)
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    v[q].x += x[t][q].x;
-                                    v[q].y += x[t][q].y;
-                                    v[q].z += x[t][q].z;
-                                    v[q].w += x[t][q].w;
-                                }
-                        }
-#pragma unroll 1
-                        for (; sl < w.nparts; ++sl) {
-                            float4 x[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                x[q] = in[q] ? __ldcg(b4 + sl * slice4 + off[q])
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                v[q].x += x[q].x;
-                                v[q].y += x[q].y;
-                                v[q].z += x[q].z;
-                                v[q].w += x[q].w;
-                            }
+                                for (int j = 0; j < 32; ++j) v[h][j] += x[h][j];
                         }
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (!in[q]) continue;
-                            const int r = off[q] / (BN / 4), c4 = off[q] - r * (BN / 4);
-                            float4 x = v[q];
-                            if constexpr (EPI) {
-                                const int n = gn0 + 4 * c4, nl = p.N - 1;
-                                x.x = epi_pre(p.epi, p.alpha, x.x, min(n, nl));
-                                x.y = epi_pre(p.epi, p.alpha, x.y, min(n + 1, nl));
-                                x.z = epi_pre(p.epi, p.alpha, x.z, min(n + 2, nl));
-                                x.w = epi_pre(p.epi, p.alpha, x.w, min(n + 3, nl));
-                            }
-                            store_quad(p, EPI ? 1.f : p.alpha, cmat, w.m_blk * TC_BM + r,
-                                       gn0 + 4 * c4, x);
+                        for (int h = 0; h < 2; ++h) {
+                            const int gn = gn0 + (c + h) * 32;
+                            if constexpr (EPI) apply_pre(p, gn, v[h]);
+                            const float alpha = EPI ? 1.f : p.alpha;
+                            if (p.c_tma)
+                                store_chunk_tma<B3>(p, alpha, cmat, w.bidx, &tmC, warp_stage,
+                                                    stage_seq, lane, gm - lane, gn, v[h]);
+                            else
+                                store_row_chunk(p, alpha, cmat, gm, gn, v[h]);
                         }
                     }
+                }
+                if (*last_flag) {
                     if (et == 0) p.counters[tile] = 0u;  // ready for the next launch
                 }
             }
