@@ -545,7 +545,8 @@ def run_ours(args, dist):
         line["e2e"] = {"value": dist.sum(flops_step * e2e_steps) / e2e_s / 1e12,
                        "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                       "api": "dense_gemm_02_gb300.gemm(host pinned tensors)"}
+                       "api": "dense_gemm_02_gb300.gemm(host pinned tensors) -> C ABI "
+                              "gemm_f32_host / gemm_bf16_host (pipelined copies)"}
     else:
         line["e2e"] = None
 

@@ -5,10 +5,11 @@ stride) and enqueue one library call on the current torch stream.
 ``gemm_ex`` adds transposed operands (a ``X.t()`` view is read in place)
 and the fused bias / activation epilogue; ``gemm_batched`` runs a strided
 batch of such products in one launch.
-``gemm`` additionally accepts host (CPU) tensors: it copies them to the
-device, runs the same call and copies C back, which is the end-to-end path
-a caller holding host buffers uses.  Nothing here computes: shapes, strides
-and pointers are read from the tensors and handed to the library.
+``gemm`` additionally accepts host (CPU) tensors, which it hands to the
+library's host-buffer entry points (copies pipelined with the computation):
+the end-to-end path of a caller holding host buffers.  Nothing here
+computes: shapes, strides and pointers are read from the tensors and handed
+to the library.
 """
 
 from __future__ import annotations
@@ -27,6 +28,8 @@ def _stream_handle(stream) -> int:
 def _row_major(t: torch.Tensor, name: str) -> int:
     if t.dim() != 2:
         raise ValueError(f"{name} must be 2-D")
+    if t.numel() == 0:  # no element is read: any pitch that passes the checks
+        return max(1, t.size(1))
     if t.size(1) > 1 and t.stride(1) != 1:
         raise ValueError(f"{name} must have unit column stride (row-major)")
     return max(1, t.stride(0)) if t.size(0) > 1 else max(1, t.size(1))
@@ -243,28 +246,47 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
     FP32 SGEMM, bfloat16 -> BF16 tensor-core GEMM).
 
     Device tensors are used in place and the call returns without
-    synchronising.  Host tensors are copied to ``device`` (asynchronously
-    when pinned; C only if beta != 0), the product is computed there, and
-    the result is copied back into ``out`` (or C, or a new pinned tensor);
-    the call returns after that copy has completed.
+    synchronising.  Host tensors go through the library's host-buffer entry
+    points (gemm_f32_host / gemm_bf16_host) on ``device``: the library copies
+    them in row blocks, computing each block as it lands and copying it back
+    while the next computes, and the call returns once the result is in
+    ``out`` (or C, or a new pinned tensor).  Pinned host tensors give the
+    full copy bandwidth.
     """
     if A.is_cuda:
         return _dispatch(A, B, C, alpha, beta, out_dtype, stream)
-    s = torch.cuda.current_stream() if stream is None else stream
-    with torch.cuda.stream(s):
-        dA = A.to(device, non_blocking=True)
-        dB = B.to(device, non_blocking=True)
-        dC = C.to(device, non_blocking=True) if (C is not None and beta != 0.0) else None
-        if dC is None and C is not None:
-            od = C.dtype
+    if A.dtype != B.dtype or A.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("A and B must both be float32 or both bfloat16")
+    if B.is_cuda or (C is not None and C.is_cuda) or (out is not None and out.is_cuda):
+        raise TypeError("host-buffer call: A, B, C and out must all be host tensors")
+    M, N, K = _shapes(A, B, C)
+    if A.dtype == torch.float32:
+        od = torch.float32
+    else:
+        od = out_dtype or (C.dtype if C is not None else torch.bfloat16)
+    if od not in (torch.float32, torch.bfloat16):
+        raise TypeError("the output must be float32 or bfloat16")
+    if out is None:
+        out = C if C is not None else torch.empty((M, N), dtype=od, pin_memory=True)
+    if tuple(out.shape) != (M, N) or out.dtype != od:
+        raise ValueError(f"out must be {(M, N)} of {od}")
+    if C is not None and beta != 0.0 and out.data_ptr() != C.data_ptr():
+        out.copy_(C)  # the library updates C in place
+    A = A if (A.dim() == 2 and (A.size(1) <= 1 or A.stride(1) == 1)) else A.contiguous()
+    B = B if (B.dim() == 2 and (B.size(1) <= 1 or B.stride(1) == 1)) else B.contiguous()
+    ldo = _row_major(out, "out")
+    with torch.cuda.device(device):
+        if A.dtype == torch.float32:
+            rc = _b.gemm_f32_host(M, N, K, float(alpha), A.data_ptr(), _row_major(A, "A"),
+                                  B.data_ptr(), _row_major(B, "B"), float(beta), out.data_ptr(),
+                                  ldo)
+            _b.check(rc, "gemm_f32_host")
         else:
-            od = out_dtype
-        dC = _dispatch(dA, dB, dC, alpha, beta, od, s)
-        if out is None:
-            out = C if C is not None else torch.empty(dC.shape, dtype=dC.dtype,
-                                                      pin_memory=True)
-        out.copy_(dC, non_blocking=True)
-    s.synchronize()
+            c_type = _b.GEMM_OUT_F32 if od == torch.float32 else _b.GEMM_OUT_BF16
+            rc = _b.gemm_bf16_host(M, N, K, float(alpha), A.data_ptr(), _row_major(A, "A"),
+                                   B.data_ptr(), _row_major(B, "B"), float(beta), out.data_ptr(),
+                                   ldo, c_type)
+            _b.check(rc, "gemm_bf16_host")
     return out
 
 

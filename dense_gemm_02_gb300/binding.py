@@ -57,6 +57,9 @@ SIGNATURES = {
                                  _f32, _vp, _i64, _i64, _int, ctypes.POINTER(GemmOpts), _vp]),
     "gemm_f32_batched": (_int, [_i64, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64, _i64,
                                 _f32, _vp, _i64, _i64, ctypes.POINTER(GemmOpts), _vp]),
+    "gemm_f32_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64]),
+    "gemm_bf16_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
+                              _int]),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_get_device_fault_info": (_i64, []),
     "gemm_status_string": (_cp, [_int]),
@@ -162,6 +165,16 @@ def gemm_f32_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, 
     ptr = ctypes.byref(opts) if opts is not None else None
     return lib().gemm_f32_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,
                                   beta, C, ldc, stride_c, ptr, stream)
+
+
+def gemm_f32_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:
+    """Raw call of the host-buffer FP32 GEMM; A, B, C are host addresses."""
+    return lib().gemm_f32_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
+
+
+def gemm_bf16_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type) -> int:
+    """Raw call of the host-buffer BF16 GEMM; A, B, C are host addresses."""
+    return lib().gemm_bf16_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type)
 
 
 def get_device_status(stream=None) -> int:

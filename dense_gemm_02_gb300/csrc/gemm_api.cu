@@ -528,6 +528,12 @@ extern "C" int gemm_shutdown(void) {
         if (w->ws) cudaFree(w->ws);
         if (w->counters) cudaFree(w->counters);
     }
+    if (st.host) {
+        for (cudaEvent_t e : st.host->events) cudaEventDestroy(e);
+        for (cudaStream_t s : {st.host->in, st.host->compute, st.host->out})
+            if (s) cudaStreamDestroy(s);
+        if (st.host->buf) cudaFree(st.host->buf);
+    }
     st = DeviceState{};
     return GEMM_OK;
 }

@@ -39,12 +39,23 @@ struct Workspace {
     size_t counters_n = 0;
 };
 
+// State of the host-buffer entry points on one device: copy-in, compute and
+// copy-out streams, their events, and one device staging allocation for A,
+// B and C, grown on demand and kept.
+struct HostPipe {
+    cudaStream_t in = nullptr, compute = nullptr, out = nullptr;
+    std::vector<cudaEvent_t> events;
+    void *buf = nullptr;
+    size_t bytes = 0;
+};
+
 // Per-device library state, created on the first call on a device.
 struct DeviceState {
     int device = -1;
     int sm_count = 0;
     unsigned long long *fault_word = nullptr;  // device, 8 bytes
     std::vector<std::unique_ptr<Workspace>> workspaces;  // one per stream used
+    std::unique_ptr<HostPipe> host;                      // gemm_*_host, on first use
 };
 
 // Returns the state of the current device (creating it), or an error.

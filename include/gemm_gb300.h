@@ -199,6 +199,26 @@ GEMM_API int gemm_f32_batched(int64_t batch, int64_t M, int64_t N, int64_t K, fl
                               int64_t stride_c, const gemm_opts_t *opts, void *stream);
 
 /*
+ * Host-buffer GEMMs: the same products with A, B and C in HOST memory
+ * (pinned memory gives the full copy bandwidth; pageable memory works).  The
+ * library copies B and then A (and C when beta != 0) to the device in row
+ * blocks, computes each block as soon as its rows have landed and copies it
+ * back while the next computes (copy-in, compute and copy-out streams of a
+ * per-device pipeline), and returns when C holds the result.  Device staging
+ * buffers are library-owned, allocated on first use, grown when a call needs
+ * more and kept until gemm_shutdown().  One host-buffer call runs at a time
+ * (others wait).  Argument rules as gemm_f32 / gemm_bf16 (C may not overlap
+ * A or B in host memory); a device pipeline fault returns
+ * GEMM_ERR_DEVICE_TIMEOUT, as gemm_get_device_status() would.
+ */
+GEMM_API int gemm_f32_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
+                           int64_t lda, const float *B, int64_t ldb, float beta, float *C,
+                           int64_t ldc);
+GEMM_API int gemm_bf16_host(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A,
+                            int64_t lda, const uint16_t *B, int64_t ldb, float beta, void *C,
+                            int64_t ldc, int c_type);
+
+/*
  * Allocation-free BF16 GEMM.  The source pages have no counterpart: this is
  * an interface for callers that cannot call cudaMalloc at all, for example
  * code that runs inside a host whose device memory is fully owned by its own
