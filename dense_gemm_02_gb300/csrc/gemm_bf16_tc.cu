@@ -111,6 +111,11 @@ struct TcParams {
     // c_bstride elements after C.
     int tiles_per_batch, a_bmul, b_bmul;
     long long c_bstride;
+    // Small M (one 128-row block, single-CTA kernel): A is loaded as
+    // a_rows rows (a multiple of 8 covering M) instead of 128; the MMA still
+    // reads 128 rows, the rest being stale shared memory whose products land
+    // in accumulator rows past M, which are never stored.
+    int a_rows;
 };
 
 // Shared-memory matrix descriptor of tcgen05 (PTX ISA, "matrix descriptor"):
@@ -518,7 +523,11 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
     for (int ui = 0; ok && cta_unit<BN>(p, ui, w); ++ui) {
         if (w.n0 >= p.N) continue;  // sub-tile wholly past the N edge
         const int boxes = w.width / 64;
-        const uint32_t tx = Cfg::A_BYTES + boxes * Cfg::B_BOX_BYTES;
+        // A bytes per stage: a_rows rows of 64 K values (K-major), or the
+        // one or two 64-row boxes of an MN-major A.
+        const uint32_t a_tx =
+            A_MN ? (p.a_rows > 64 ? 2u : 1u) * 8192u : (uint32_t)p.a_rows * 128u;
+        const uint32_t tx = a_tx + boxes * Cfg::B_BOX_BYTES;
         const int m0 = w.m_blk * TC_BM;
         const int ab = w.bidx * p.a_bmul, bb = w.bidx * p.b_bmul;  // batch coordinates
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
@@ -538,7 +547,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
             const int k0 = kb * TC_BK;
             if constexpr (A_MN) {
                 load_box<B3>(a_dst, tmA, &full[s], m0, k0, ab);
-                load_box<B3>(a_dst + 8192, tmA, &full[s], m0 + 64, k0, ab);
+                if (p.a_rows > 64) load_box<B3>(a_dst + 8192, tmA, &full[s], m0 + 64, k0, ab);
             } else {
                 load_box<B3>(a_dst, tmA, &full[s], k0, m0, ab);
             }
@@ -1234,7 +1243,8 @@ bool make_ab_maps(CUtensorMap *ta, CUtensorMap *tb, const TcParams &p, const uin
     const uint64_t db = b3 ? (p.b_bmul ? (uint64_t)o.batch : 1) : 0;
     const uint64_t sa = (uint64_t)o.stride_a, sb = (uint64_t)o.stride_b;
     const bool ok_a = p.a_mn ? make_map(ta, A, M, K, (uint64_t)lda, 64, TC_BK, da, sa)
-                             : make_map(ta, A, K, M, (uint64_t)lda, TC_BK, TC_BM, da, sa);
+                             : make_map(ta, A, K, M, (uint64_t)lda, TC_BK, (uint32_t)p.a_rows,
+                                        da, sa);
     const bool ok_b = p.b_kmaj ? make_map(tb, B, K, N, (uint64_t)ldb, TC_BK, 64, db, sb)
                                : make_map(tb, B, N, K, (uint64_t)ldb, 64, TC_BK, db, sb);
     return ok_a && ok_b;
@@ -1583,6 +1593,8 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
         const int num_kb = (K + TC_BK - 1) / TC_BK;
         pair = !(tiles1 * 2 <= sm_count && num_kb >= 8);
     }
+    p.a_rows = TC_BM;
+    if (!pair && M <= TC_BM) p.a_rows = std::max(8, (M + 7) / 8 * 8);
     if (pair) return launch_tc2(device, p, A, lda, B, ldb, o, stream);
     return bn == 256 ? launch_tc<256>(device, sm_count, st, ext, p, A, lda, B, ldb, o, stream)
                      : launch_tc<128>(device, sm_count, st, ext, p, A, lda, B, ldb, o, stream);
