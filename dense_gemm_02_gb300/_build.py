@@ -3,7 +3,8 @@
 Each .cu file is compiled on its own thread (they are independent
 translation units) and the objects are linked into one shared library under
 ``dense_gemm_02_gb300/_lib``.  A rebuild happens only when a source or header
-is newer than the library.
+is newer than the library, and then recompiles only the objects older than
+their source or than any header.
 """
 
 from __future__ import annotations
@@ -43,9 +44,7 @@ def sources():
 
 
 def _deps():
-    return (sources() + glob.glob(os.path.join(CSRC, "*.cuh"))
-            + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
-            + [os.path.abspath(__file__)])
+    return sources() + _headers()
 
 
 def up_to_date() -> bool:
@@ -55,8 +54,23 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
+def _headers():
+    return (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
+            + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
+
+
+def _obj_path(src: str) -> str:
+    return os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+
+
+def _obj_current(src: str, newest_header: float) -> bool:
+    obj = _obj_path(src)
+    return os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src),
+                                                                newest_header)
+
+
 def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+    obj = _obj_path(src)
     cmd = [nvcc(), *ARCH_FLAGS, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd[1:1] = ["-Xptxas", "-v"]
@@ -75,8 +89,13 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     os.makedirs(OBJ_DIR, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     srcs = sources()
-    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
+    # Objects newer than their source and every header are reused.
+    newest_header = max(os.path.getmtime(h) for h in _headers())
+    stale = [s for s in srcs if force or verbose_ptxas or not _obj_current(s, newest_header)]
+    if stale:
+        with cf.ThreadPoolExecutor(max_workers=max(1, min(len(stale), os.cpu_count() or 1))) as ex:
+            list(ex.map(lambda s: _compile(s, verbose_ptxas), stale))
+    objs = [_obj_path(s) for s in srcs]
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH_FLAGS, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)

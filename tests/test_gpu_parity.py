@@ -444,3 +444,26 @@ def test_watchdog_reports_a_withheld_stage_and_recovers():
     assert g.binding.get_device_status() == g.binding.GEMM_OK
     ref = oracle.round_f32(oracle.gemm(A, B))
     assert np.array_equal(C.cpu().numpy(), ref)
+
+
+def test_sgemm_watchdog_reports_a_withheld_stage_and_recovers():
+    M, N, K = 512, 512, 1024
+    A = gi.draw("integer", 18, 0, (M, K))
+    B = gi.draw("integer", 18, 1, (K, N))
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    old = g.get_config("watchdog_ms")
+    g.set_config("watchdog_ms", 200)
+    g.set_config("fault_inject", 1)
+    try:
+        g.sgemm(dA, dB, C)
+        rc = g.binding.get_device_status()
+    finally:
+        g.set_config("fault_inject", 0)
+        g.set_config("watchdog_ms", old)
+    assert g.binding.last_kernel() == "sgemm_tma"
+    assert rc == g.binding.GEMM_ERR_DEVICE_TIMEOUT
+    assert g.binding.get_device_fault_info() & 0xFF == 4  # the SGEMM's role code
+    g.sgemm(dA, dB, C)
+    assert g.binding.get_device_status() == g.binding.GEMM_OK
+    assert np.array_equal(C.cpu().numpy(), oracle.round_f32(oracle.gemm(A, B)))
