@@ -24,6 +24,7 @@ std::atomic<int64_t> g_tail_split_off{0};
 std::atomic<int64_t> g_raster_group{0};
 std::atomic<int64_t> g_cta_pair{0};
 std::atomic<int64_t> g_stream_k{0};
+std::atomic<int64_t> g_pair_limit{0};
 std::atomic<int64_t> g_last_fault{0};
 
 std::mutex g_state_mu;
@@ -147,7 +148,8 @@ int stream_workspace(DeviceState *st, cudaStream_t stream, size_t ws_bytes, size
 RuntimeConfig runtime_config() {
     return RuntimeConfig{g_watchdog_ms.load(), g_force_path.load(), g_fault_inject.load(),
                          g_split_k.load(),      g_bf16_tile_n.load(), g_tail_split_off.load(),
-                         g_raster_group.load(), g_cta_pair.load(), g_stream_k.load()};
+                         g_raster_group.load(), g_cta_pair.load(), g_stream_k.load(),
+                         g_pair_limit.load()};
 }
 
 void consume_fault_inject() { g_fault_inject.store(0); }
@@ -492,6 +494,9 @@ extern "C" int gemm_set_config(const char *key, int64_t value) {
     } else if (!strcmp(key, "stream_k")) {
         if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
         g_stream_k.store(value);
+    } else if (!strcmp(key, "pair_limit")) {
+        if (value < 0 || value > 1024) return GEMM_ERR_INVALID_ARG;
+        g_pair_limit.store(value);
     } else {
         return GEMM_ERR_INVALID_ARG;
     }
@@ -509,6 +514,7 @@ extern "C" int gemm_get_config(const char *key, int64_t *value) {
     else if (!strcmp(key, "raster_group")) *value = g_raster_group.load();
     else if (!strcmp(key, "cta_pair")) *value = g_cta_pair.load();
     else if (!strcmp(key, "stream_k")) *value = g_stream_k.load();
+    else if (!strcmp(key, "pair_limit")) *value = g_pair_limit.load();
     else return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }

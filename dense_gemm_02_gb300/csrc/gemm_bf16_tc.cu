@@ -714,11 +714,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the loop (every lane waits on the same
+        // barriers and takes the same branches); one elected lane issues
+        // each MMA and commit.
+        {
             // Operand tiles as described at operand_layout.  The loop below
-            // only adds offsets to these descriptors: a single issuing thread
-            // must spend as few instructions as possible between MMAs to keep
-            // the tensor pipe fed.
+            // only adds offsets to these descriptors: the issuing warp must
+            // spend as few instructions as possible between MMAs to keep the
+            // tensor pipe fed.
             const OperandLayout la = operand_layout(p.a_mn), lb = operand_layout(!p.b_kmaj);
             const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), la.lbo, 1024);
             const uint64_t b_desc0 = smem_desc_sw128(smem_addr(sB), lb.lbo, 1024);
@@ -732,8 +735,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t idesc = idesc_bf16_f32(w.width, TC_BM, p.a_mn, p.b_kmaj);
                 const uint32_t b = local & 1u, use = local >> 1;
                 ++local;
-                if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
-                    record_fault(p, abort_flag, kRoleMma, 0xfe, w.tile);
+                const bool got = mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns);
+                if (__any_sync(0xffffffffu, !got)) {
+                    if (lane == 0) record_fault(p, abort_flag, kRoleMma, 0xfe, w.tile);
                     ok = false;
                     break;
                 }
@@ -741,19 +745,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t d_tmem = tmem_base + b * BN;
                 uint32_t acc = 0;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&full[s], ph, abort_flag, p.timeout_ns)) {
-                        record_fault(p, abort_flag, kRoleMma, s, w.tile);
+                    const bool ready = mbar_wait(&full[s], ph, abort_flag, p.timeout_ns);
+                    if (__any_sync(0xffffffffu, !ready)) {
+                        if (lane == 0) record_fault(p, abort_flag, kRoleMma, s, w.tile);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const uint64_t ad = desc_add(a_desc0, s * Cfg::A_BYTES);
                     const uint64_t bd = desc_add(b_desc0, s * Cfg::B_BYTES);
-                    umma_f16(d_tmem, ad, bd, idesc, acc);
-                    umma_f16(d_tmem, ad + a1, bd + b1, idesc, 1u);
-                    umma_f16(d_tmem, ad + a2, bd + b2, idesc, 1u);
-                    umma_f16(d_tmem, ad + a3, bd + b3, idesc, 1u);
-                    umma_commit(&empty[s]);  // frees the stage once these MMAs finish
+                    umma_f16_elect(d_tmem, ad, bd, idesc, acc);
+                    umma_f16_elect(d_tmem, ad + a1, bd + b1, idesc, 1u);
+                    umma_f16_elect(d_tmem, ad + a2, bd + b2, idesc, 1u);
+                    umma_f16_elect(d_tmem, ad + a3, bd + b3, idesc, 1u);
+                    umma_commit_elect(&empty[s]);  // frees the stage once these MMAs finish
                     acc = 1u;
                     if (++s == (uint32_t)S) {
                         s = 0;
@@ -761,10 +766,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit(&tfull[b]);  // accumulator b is complete
+                umma_commit_elect(&tfull[b]);  // accumulator b is complete
             }
-            // All MMAs issued here must finish before TMEM is released.
-            umma_commit(drain);
+            // The elected lane's MMAs must finish before TMEM is released.
+            umma_commit_elect(drain);
             mbar_wait(drain, 0, abort_flag, p.timeout_ns, true);
         }
         __syncwarp();
@@ -1092,7 +1097,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
-        if (lane == 0 && leader) {
+        // The whole warp runs the loop (every lane waits on the same
+        // barriers and takes the same branches); one elected lane issues
+        // each MMA and commit.
+        if (leader) {
             // Same descriptor scheme as the single-CTA kernel (offsets only).
             const OperandLayout la = operand_layout(p.a_mn), lb = operand_layout(!p.b_kmaj);
             const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), la.lbo, 1024);
@@ -1107,8 +1115,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t idesc = idesc_bf16_f32(w.width, 2 * TC_BM, p.a_mn, p.b_kmaj);
                 const uint32_t b = local & 1u, use = local >> 1;
                 ++local;
-                if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns)) {
-                    record_fault(p, abort_flag, kRoleMma, 0xfe, w.tile);
+                const bool got = mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns);
+                if (__any_sync(0xffffffffu, !got)) {
+                    if (lane == 0) record_fault(p, abort_flag, kRoleMma, 0xfe, w.tile);
                     ok = false;
                     break;
                 }
@@ -1116,19 +1125,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t d_tmem = tmem_base + b * BN;
                 uint32_t acc = 0;
                 for (int kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!mbar_wait(&full[s], ph, abort_flag, p.timeout_ns)) {
-                        record_fault(p, abort_flag, kRoleMma, s, w.tile);
+                    const bool ready = mbar_wait(&full[s], ph, abort_flag, p.timeout_ns);
+                    if (__any_sync(0xffffffffu, !ready)) {
+                        if (lane == 0) record_fault(p, abort_flag, kRoleMma, s, w.tile);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const uint64_t ad = desc_add(a_desc0, s * Cfg::A_BYTES);
                     const uint64_t bd = desc_add(b_desc0, s * Cfg::B_BYTES);
-                    umma_f16_pair(d_tmem, ad, bd, idesc, acc);
-                    umma_f16_pair(d_tmem, ad + a1, bd + b1, idesc, 1u);
-                    umma_f16_pair(d_tmem, ad + a2, bd + b2, idesc, 1u);
-                    umma_f16_pair(d_tmem, ad + a3, bd + b3, idesc, 1u);
-                    umma_commit_pair(&empty[s], 0x3);  // frees stage s in both CTAs
+                    umma_f16_pair_elect(d_tmem, ad, bd, idesc, acc);
+                    umma_f16_pair_elect(d_tmem, ad + a1, bd + b1, idesc, 1u);
+                    umma_f16_pair_elect(d_tmem, ad + a2, bd + b2, idesc, 1u);
+                    umma_f16_pair_elect(d_tmem, ad + a3, bd + b3, idesc, 1u);
+                    umma_commit_pair_elect(&empty[s], 0x3);  // frees stage s in both CTAs
                     acc = 1u;
                     if (++s == (uint32_t)S) {
                         s = 0;
@@ -1136,9 +1146,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(&tfull[b], 0x3);  // accumulator b complete in both CTAs
+                umma_commit_pair_elect(&tfull[b], 0x3);  // accumulator b complete in both CTAs
             }
-            umma_commit_pair(drain, 0x1);
+            // The elected lane's MMAs must finish before TMEM is released.
+            umma_commit_pair_elect(drain, 0x1);
             mbar_wait(drain, 0, abort_flag, p.timeout_ns, true);
         }
         __syncwarp();
@@ -1465,12 +1476,13 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
                 return GEMM_ERR_CUDA;
         attr_done[device] = true;
     }
-    const int pairs_max = max_resident_pairs(device);
+    const RuntimeConfig cfg = runtime_config();
+    int pairs_max = max_resident_pairs(device);
     if (pairs_max <= 0) return GEMM_ERR_CUDA;
+    if (cfg.pair_limit > 0 && cfg.pair_limit < pairs_max) pairs_max = (int)cfg.pair_limit;
     alignas(64) CUtensorMap ta, tb, tc;
     if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb, o)) return GEMM_ERR_CUDA;
     if (!make_c_map(&tc, p, o.batch)) return GEMM_ERR_CUDA;
-    const RuntimeConfig cfg = runtime_config();
     p.num_m_blk = (p.M + 2 * TC_BM - 1) / (2 * TC_BM);  // 256-row pair tiles
     p.num_n_blk = (p.N + Cfg::BN - 1) / Cfg::BN;
     p.num_kb = (p.K + TC_BK - 1) / TC_BK;
@@ -1494,7 +1506,12 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
         p.group_m = (int)g;
     }
     // Partial last wave: cut its tiles into two 128-column halves when that
-    // still leaves every half a pair of its own.
+    // still leaves every half a pair of its own.  (Dealing the tail tiles'
+    // K iterations out to all pairs instead, stream-K style, was measured
+    // slower on GB300: 4096^3 94 us against 83 us.  The pieces' MMAs take
+    // 8-12 us, but the last piece of each tile to arrive must read three
+    // or four 128 KiB fp32 partials per CTA, and with the loads one SM keeps
+    // in flight that takes 7-10 us.)
     p.tiles_main = (int)tiles;
     p.tail_split = 1;
     {

@@ -78,6 +78,7 @@ struct RuntimeConfig {
     int64_t raster_group;
     int64_t cta_pair;
     int64_t stream_k;
+    int64_t pair_limit;
 };
 RuntimeConfig runtime_config();
 void consume_fault_inject();

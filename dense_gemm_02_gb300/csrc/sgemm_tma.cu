@@ -119,11 +119,10 @@ __global__ void __launch_bounds__(TTHREADS, 2)
         tma_load_3d(st, &tmA, &full[s], (kt0 + kt) * TBK, m0, ab);
         tma_load_3d(st + TA_BYTES, &tmB, &full[s], n0, (kt0 + kt) * TBK, bb);
     };
-    const bool withhold = p.fault_inject && blockIdx.x == 0;
     int issued = 0;
     if (tid == 0)
         for (; issued < TSTAGES - 1 && issued < KT; ++issued)
-            if (!(withhold && issued == 0)) issue(issued);
+            if (!(p.fault_inject && blockIdx.x == 0 && issued == 0)) issue(issued);
 
     float acc[8][8];
 #pragma unroll
@@ -194,7 +193,7 @@ __global__ void __launch_bounds__(TTHREADS, 2)
                                                      (unsigned)blockIdx.x));
             // Let the copies still in flight land before the CTA exits.
             for (int j = kt; j < issued; ++j)
-                if (!(withhold && j == 0))
+                if (!(p.fault_inject && blockIdx.x == 0 && j == 0))
                     mbar_wait(&full[j % TSTAGES], (uint32_t)((j / TSTAGES) & 1), never,
                               p.timeout_ns, true);
         }
@@ -330,6 +329,7 @@ int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const fl
     p.fault_word = st->fault_word;
     p.timeout_ns = (unsigned long long)runtime_config().watchdog_ms * 1000000ull;
     p.fault_inject = runtime_config().fault_inject ? 1 : 0;
+    if (p.fault_inject) consume_fault_inject();
     const long long tiles_per_batch = (long long)p.num_m_blk * p.num_n_blk;
     const long long tiles = tiles_per_batch * batch;
     if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;

@@ -280,13 +280,14 @@ GEMM_API const char *gemm_status_string(int status);
  *   "force_path"    0 auto, 1 force the non-TMA kernels (cp.async SGEMM,
  *                   generic BF16 kernel),
  *                   2 force the tcgen05 kernel (fails on misaligned input)
- *   "fault_inject"  1: the next tcgen05 launch withholds one pipeline stage so
- *                   its waits run out (tests the watchdog); resets itself
+ *   "fault_inject"  1: the next tcgen05 or FP32 TMA launch withholds one
+ *                   pipeline stage so its waits run out (tests the
+ *                   watchdog); resets itself
  *   "split_k"       0 auto, else the number of K slices for the tcgen05 kernel
  *   "bf16_tile_n"   0 auto, else 128 or 256 (tcgen05 tile width)
- *   "tail_split_off" 1: do not cut the tiles of the last partial wave into
- *                   narrower sub-tiles (tcgen05 kernel) or along K (FP32
- *                   TMA kernel); 0 (default) cuts them
+ *   "tail_split_off" 1: leave the tiles of the last partial wave whole;
+ *                   0 (default) cuts them: into narrower sub-tiles
+ *                   (tcgen05 kernels) or along K (FP32 TMA kernel)
  *   "stream_k"      1: when a tcgen05 GEMM has few tiles and a long K, deal
  *                   all K iterations out to the SMs in equal ranges
  *                   (stream-K); 0 (default): equal K slices per tile
@@ -294,6 +295,9 @@ GEMM_API const char *gemm_status_string(int status);
  *                   for CTA pairs) per raster band of the tcgen05 kernel
  *   "cta_pair"      0 auto, 1 single-CTA tcgen05 kernel only, 2 always the
  *                   CTA-pair (2-SM, cta_group::2) kernel
+ *   "pair_limit"    0 all resident pairs, else at most this many CTA pairs
+ *                   (leaves SMs free for other work; tests use it to reach
+ *                   the tail paths at small sizes)
  * Returns GEMM_OK or GEMM_ERR_INVALID_ARG for an unknown key or value.
  */
 GEMM_API int gemm_set_config(const char *key, int64_t value);

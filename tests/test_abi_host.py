@@ -160,6 +160,18 @@ def test_config_keys(lib):
         b.set_config("no_such_key", 1)
     with pytest.raises(b.GemmError):
         b.set_config("bf16_tile_n", 96)
+    # every documented key round-trips its default and rejects a bad value
+    for key, bad in (("force_path", 3), ("fault_inject", 2), ("split_k", 65), ("bf16_tile_n", 64),
+                     ("tail_split_off", 2), ("stream_k", 2), ("raster_group", -1),
+                     ("cta_pair", 3), ("pair_limit", -1)):
+        v = b.get_config(key)
+        b.set_config(key, v)
+        with pytest.raises(b.GemmError):
+            b.set_config(key, bad)
+        assert b.get_config(key) == v
+    b.set_config("pair_limit", 4)
+    assert b.get_config("pair_limit") == 4
+    b.set_config("pair_limit", 0)
     assert b.last_kernel() in {"none", "sgemm_simt", "sgemm_tma", "bf16_tcgen05", "bf16_simt",
                                 "f32_simt", "scale_c"}
 
