@@ -59,16 +59,21 @@ constexpr int TC_EPI_BAR = 1;        // named barrier id of the epilogue warps
 constexpr int kEpiChunkBytes = 4096;
 constexpr int kEpiStagingBytes = 4 * 2 * kEpiChunkBytes;
 
+// The operand ring of the single-CTA kernel is packed: a stage holds the A
+// rows the launch loads (a_slot bytes: 16 KiB for 128 rows, less for a
+// small M) followed by the B tile, so small-M launches fit more stages in
+// the same bytes and keep more loads in flight (up to MAX_STAGES).
 template <int BN>
 struct TcCfg {
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;  // with 128 A rows
+    static constexpr int MAX_STAGES = 12;
     static constexpr int A_BYTES = TC_BM * TC_BK * 2;  // 16 KiB
     static constexpr int B_BYTES = BN * TC_BK * 2;     // 32 KiB at BN = 256
     static constexpr int B_BOX_BYTES = 64 * TC_BK * 2; // one 64-column B box, 8 KiB
-    static constexpr int OFF_B = STAGES * A_BYTES;
-    static constexpr int OFF_STAGE = OFF_B + STAGES * B_BYTES;  // epilogue staging
+    static constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);
+    static constexpr int OFF_STAGE = RING_BYTES;  // epilogue staging
     static constexpr int OFF_BAR = OFF_STAGE + kEpiStagingBytes;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
+    static constexpr int NUM_BARS = 2 * MAX_STAGES + 5;  // full, empty, tfull[2], tempty[2], drain
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -116,6 +121,9 @@ struct TcParams {
     // reads 128 rows, the rest being stale shared memory whose products land
     // in accumulator rows past M, which are never stored.
     int a_rows;
+    // Packed operand ring (single-CTA kernel): `stages` stages of
+    // stage_bytes, each a_slot bytes of A followed by the B tile.
+    int stages, stage_bytes, a_slot;
 };
 
 // Shared-memory matrix descriptor of tcgen05 (PTX ISA, "matrix descriptor"):
@@ -431,60 +439,6 @@ __device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha, 
     ++seq;
 }
 
-// Stores C[gm][gn..gn+3] = alpha * acc + beta * C (one 16-byte fp32 or
-// 8-byte bf16 store when C rows are 16-byte aligned and the four columns
-// are inside C).
-__device__ __forceinline__ void store_quad(const TcParams &p, float alpha, void *C, int gm, int gn,
-                                           float4 acc) {
-    if (gm >= p.M || gn >= p.N) return;
-    const float beta = p.beta;
-    const float a[4] = {acc.x, acc.y, acc.z, acc.w};
-    float o[4];
-    if (p.c_f32) {
-        float *crow = static_cast<float *>(C) + (long long)gm * p.ldc;
-        if (p.c_vec && gn + 4 <= p.N) {
-            float4 *dst = reinterpret_cast<float4 *>(crow + gn);
-            const float4 c = (beta != 0.f) ? *dst : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float cv[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) o[j] = beta != 0.f ? fmaf(alpha, a[j], beta * cv[j]) : alpha * a[j];
-            *dst = make_float4(o[0], o[1], o[2], o[3]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (gn + j < p.N)
-                    crow[gn + j] = beta != 0.f ? fmaf(alpha, a[j], beta * crow[gn + j]) : alpha * a[j];
-        }
-    } else {
-        uint16_t *crow = static_cast<uint16_t *>(C) + (long long)gm * p.ldc;
-        if (p.c_vec && gn + 4 <= p.N) {
-            uint2 *dst = reinterpret_cast<uint2 *>(crow + gn);
-            uint2 c = make_uint2(0u, 0u);
-            if (beta != 0.f) c = *dst;
-            const uint32_t cw[2] = {c.x, c.y};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t h = (j & 1) ? (cw[j >> 1] >> 16) : (cw[j >> 1] & 0xFFFFu);
-                o[j] = beta != 0.f ? fmaf(alpha, a[j], beta * bf16_bits_to_float(h)) : alpha * a[j];
-            }
-            __nv_bfloat162 p0 = __floats2bfloat162_rn(o[0], o[1]);
-            __nv_bfloat162 p1 = __floats2bfloat162_rn(o[2], o[3]);
-            *dst = make_uint2(*reinterpret_cast<uint32_t *>(&p0), *reinterpret_cast<uint32_t *>(&p1));
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (gn + j < p.N) {
-                    const float v = beta != 0.f ? fmaf(alpha, a[j], beta * bf16_bits_to_float(crow[gn + j]))
-                                                : alpha * a[j];
-                    __nv_bfloat16 hb = __float2bfloat16_rn(v);
-                    crow[gn + j] = *reinterpret_cast<uint16_t *>(&hb);
-                }
-            }
-        }
-    }
-}
-
-
 // One TMA box of an operand: 3-D maps (B3) take the batch coordinate.
 template <bool B3>
 __device__ __forceinline__ void load_box(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
@@ -511,12 +465,12 @@ __device__ __forceinline__ void load_box_pair(void *dst, const CUtensorMap *map,
 // with the same bytes.
 template <int BN, bool A_MN, bool B_KM, bool B3>
 __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap *tmA,
-                                            const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
+                                            const CUtensorMap *tmB, uint8_t *ring,
                                             uint64_t *full, uint64_t *empty,
                                             volatile int *abort_flag) {
     using Cfg = TcCfg<BN>;
-    constexpr int S = Cfg::STAGES;
-    uint32_t it = 0;
+    const uint32_t S = (uint32_t)p.stages;
+    uint32_t it = 0, s = 0, ph = 0;
     int withheld = -1;
     bool ok = true;
     Unit w;
@@ -531,10 +485,13 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
         const int m0 = w.m_blk * TC_BM;
         const int ab = w.bidx * p.a_bmul, bb = w.bidx * p.b_bmul;  // batch coordinates
         for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (it / S) & 1u;
-            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) {
-                record_fault(p, abort_flag, kRoleProducer, s, w.tile);
+            const uint32_t cur = s, cur_ph = ph;
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+            if (!mbar_wait(&empty[cur], cur_ph ^ 1u, abort_flag, p.timeout_ns)) {
+                record_fault(p, abort_flag, kRoleProducer, cur, w.tile);
                 ok = false;
                 break;
             }
@@ -542,28 +499,28 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
                 withheld = 0;  // test hook: this stage is never filled
                 continue;
             }
-            mbar_arrive_expect_tx(&full[s], tx);
-            uint8_t *a_dst = sA + s * Cfg::A_BYTES;
+            mbar_arrive_expect_tx(&full[cur], tx);
+            uint8_t *a_dst = ring + cur * (uint32_t)p.stage_bytes;
+            uint8_t *b_dst = a_dst + p.a_slot;
             const int k0 = kb * TC_BK;
             if constexpr (A_MN) {
-                load_box<B3>(a_dst, tmA, &full[s], m0, k0, ab);
-                if (p.a_rows > 64) load_box<B3>(a_dst + 8192, tmA, &full[s], m0 + 64, k0, ab);
+                load_box<B3>(a_dst, tmA, &full[cur], m0, k0, ab);
+                if (p.a_rows > 64) load_box<B3>(a_dst + 8192, tmA, &full[cur], m0 + 64, k0, ab);
             } else {
-                load_box<B3>(a_dst, tmA, &full[s], k0, m0, ab);
+                load_box<B3>(a_dst, tmA, &full[cur], k0, m0, ab);
             }
-            uint8_t *b_dst = sB + s * Cfg::B_BYTES;
             for (int j = 0; j < boxes; ++j) {
                 if constexpr (B_KM)
-                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[s], k0, w.n0 + j * 64,
-                                 bb);
+                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[cur], k0,
+                                 w.n0 + j * 64, bb);
                 else
-                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[s], w.n0 + j * 64, k0,
-                                 bb);
+                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[cur], w.n0 + j * 64,
+                                 k0, bb);
             }
         }
     }
     // Let every copy started here land before the CTA can exit.
-    const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+    const uint32_t first = it > S ? it - S : 0u;
     for (uint32_t i = first; i < it; ++i) {
         if ((int)i == withheld) continue;
         mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
@@ -574,17 +531,17 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
 // branches in this single thread measurably slow the pipeline.
 template <int BN, bool B3>
 __device__ __forceinline__ void tc_produce_layout(const TcParams &p, const CUtensorMap *tmA,
-                                                  const CUtensorMap *tmB, uint8_t *sA,
-                                                  uint8_t *sB, uint64_t *full, uint64_t *empty,
+                                                  const CUtensorMap *tmB, uint8_t *ring,
+                                                  uint64_t *full, uint64_t *empty,
                                                   volatile int *abort_flag) {
     if (!p.a_mn && !p.b_kmaj)
-        tc_producer<BN, false, false, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
+        tc_producer<BN, false, false, B3>(p, tmA, tmB, ring, full, empty, abort_flag);
     else if (!p.a_mn)
-        tc_producer<BN, false, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
+        tc_producer<BN, false, true, B3>(p, tmA, tmB, ring, full, empty, abort_flag);
     else if (!p.b_kmaj)
-        tc_producer<BN, true, false, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
+        tc_producer<BN, true, false, B3>(p, tmA, tmB, ring, full, empty, abort_flag);
     else
-        tc_producer<BN, true, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag);
+        tc_producer<BN, true, true, B3>(p, tmA, tmB, ring, full, empty, abort_flag);
 }
 
 // Loads two consecutive 32-column chunks (64 floats) of this thread's row
@@ -658,16 +615,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
     using Cfg = TcCfg<BN>;
-    constexpr int S = Cfg::STAGES;
+    constexpr int SMAX = Cfg::MAX_STAGES;
+    const uint32_t S = (uint32_t)p.stages;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzled tiles need 1024-byte aligned shared addresses.
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + Cfg::OFF_B;
+    uint8_t *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
     uint64_t *full = bars;
-    uint64_t *empty = bars + S;
-    uint64_t *tfull = bars + 2 * S;
+    uint64_t *empty = bars + SMAX;
+    uint64_t *tfull = bars + 2 * SMAX;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
@@ -679,7 +636,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
+        for (uint32_t s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -709,7 +666,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            tc_produce_layout<BN, B3>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag);
+            tc_produce_layout<BN, B3>(p, &tmA, &tmB, ring, full, empty, abort_flag);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -723,8 +680,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // spend as few instructions as possible between MMAs to keep the
             // tensor pipe fed.
             const OperandLayout la = operand_layout(p.a_mn), lb = operand_layout(!p.b_kmaj);
-            const uint64_t a_desc0 = smem_desc_sw128(smem_addr(sA), la.lbo, 1024);
-            const uint64_t b_desc0 = smem_desc_sw128(smem_addr(sB), lb.lbo, 1024);
+            const uint64_t a_desc0 = smem_desc_sw128(smem_addr(ring), la.lbo, 1024);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_addr(ring + p.a_slot), lb.lbo, 1024);
+            const uint32_t stage_bytes = (uint32_t)p.stage_bytes;
             const uint32_t a1 = la.step, a2 = 2 * la.step, a3 = 3 * la.step;
             const uint32_t b1 = lb.step, b2 = 2 * lb.step, b3 = 3 * lb.step;
             uint32_t s = 0, ph = 0, local = 0;
@@ -752,15 +710,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t ad = desc_add(a_desc0, s * Cfg::A_BYTES);
-                    const uint64_t bd = desc_add(b_desc0, s * Cfg::B_BYTES);
+                    const uint64_t ad = desc_add(a_desc0, s * stage_bytes);
+                    const uint64_t bd = desc_add(b_desc0, s * stage_bytes);
                     umma_f16_elect(d_tmem, ad, bd, idesc, acc);
                     umma_f16_elect(d_tmem, ad + a1, bd + b1, idesc, 1u);
                     umma_f16_elect(d_tmem, ad + a2, bd + b2, idesc, 1u);
                     umma_f16_elect(d_tmem, ad + a3, bd + b3, idesc, 1u);
                     umma_commit_elect(&empty[s]);  // frees the stage once these MMAs finish
                     acc = 1u;
-                    if (++s == (uint32_t)S) {
+                    if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -1421,6 +1379,10 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
             p.counters = w->counters;
         }
     }
+    // Packed ring: the A rows this launch loads, then the B tile, per stage.
+    p.a_slot = p.a_mn ? (p.a_rows > 64 ? 16384 : 8192) : p.a_rows * 128;
+    p.stage_bytes = p.a_slot + Cfg::B_BYTES;
+    p.stages = std::min(Cfg::MAX_STAGES, Cfg::RING_BYTES / p.stage_bytes);
     const int grid = p.stream_k ? (int)sk_ctas : (int)(units < sm_count ? units : sm_count);
     const int smem = Cfg::SMEM_ALLOC;
     if (o.batch > 1) {
