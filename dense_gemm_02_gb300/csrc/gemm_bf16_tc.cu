@@ -1186,6 +1186,66 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// Tensor maps encoded on this thread, most recent first in no particular
+// order: a map is plain data fixed by its arguments (base address, shape,
+// strides, box, swizzle), so a call that repeats them reuses the encoded
+// map instead of encoding it again (about a microsecond each).
+struct MapEntry {
+    bool used;
+    CUtensorMapDataType dtype;
+    cuuint32_t rank;
+    const void *base;
+    cuuint64_t dims[3];
+    cuuint64_t strides[2];
+    cuuint32_t box[3];
+    CUtensorMapSwizzle swizzle;
+    CUtensorMapL2promotion l2;
+    CUtensorMap map;
+};
+constexpr int kMapCacheSize = 16;
+thread_local MapEntry t_maps[kMapCacheSize];
+thread_local int t_next_map = 0;
+
+bool encode_cached(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank, const void *base,
+                   const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                   CUtensorMapSwizzle swizzle, CUtensorMapL2promotion l2) {
+    for (MapEntry &e : t_maps) {
+        if (!e.used || e.base != base || e.dtype != dtype || e.rank != rank ||
+            e.swizzle != swizzle || e.l2 != l2)
+            continue;
+        bool same = true;
+        for (cuuint32_t i = 0; i < rank; ++i)
+            same = same && e.dims[i] == dims[i] && e.box[i] == box[i] &&
+                   (i + 1 == rank || e.strides[i] == strides[i]);
+        if (same) {
+            *map = e.map;
+            return true;
+        }
+    }
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return false;
+    MapEntry &e = t_maps[t_next_map];
+    t_next_map = (t_next_map + 1) % kMapCacheSize;
+    e.used = true;
+    e.dtype = dtype;
+    e.rank = rank;
+    e.base = base;
+    e.swizzle = swizzle;
+    e.l2 = l2;
+    for (cuuint32_t i = 0; i < 3; ++i) {
+        e.dims[i] = i < rank ? dims[i] : 0;
+        e.box[i] = i < rank ? box[i] : 0;
+    }
+    for (cuuint32_t i = 0; i < 2; ++i) e.strides[i] = i + 1 < rank ? strides[i] : 0;
+    e.map = *map;
+    return true;
+}
+
 // 2-D bf16 tensor map over a row-major matrix: `inner` contiguous elements
 // per row, `outer` rows, `pitch` elements between rows; box of
 // box_inner x box_outer with 128-byte swizzle; out-of-range reads give 0.
@@ -1233,19 +1293,16 @@ bool make_c_map(CUtensorMap *map, TcParams &p, int64_t batch) {
         memset(map, 0, sizeof(*map));
         return true;
     }
-    auto fn = encode_fn();
-    if (!fn) return false;
     const uint64_t depth = batch > 1 ? (uint64_t)batch : 1;
     const uint64_t dstride = (uint64_t)p.c_bstride * esz;
-    cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.M, depth};
-    cuuint64_t strides[2] = {(cuuint64_t)p.ldc * esz, dstride};
-    cuuint32_t box[3] = {32, 32, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, p.c_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-              batch > 1 ? 3 : 2,
-              p.C, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              p.c_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const cuuint64_t dims[3] = {(cuuint64_t)p.N, (cuuint64_t)p.M, depth};
+    const cuuint64_t strides[2] = {(cuuint64_t)p.ldc * esz, dstride};
+    const cuuint32_t box[3] = {32, 32, 1};
+    return encode_cached(map,
+                         p.c_f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         batch > 1 ? 3 : 2, p.C, dims, strides, box,
+                         p.c_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 template <int BN>
@@ -1585,18 +1642,14 @@ bool encode_tensor_map_3d(CUtensorMap *map, CUtensorMapDataType dtype, const voi
                           uint64_t inner, uint64_t outer, uint64_t depth, uint64_t pitch_bytes,
                           uint64_t depth_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                           CUtensorMapSwizzle swizzle) {
-    auto fn = encode_fn();
-    if (!fn) return false;
     const cuuint32_t rank = depth == 0 ? 2 : 3;
     if (depth == 1)  // any valid stride: the third coordinate is always 0
         depth_stride_bytes = (pitch_bytes * (outer > 0 ? outer : 1) + 15) / 16 * 16;
-    cuuint64_t dims[3] = {inner, outer, depth};
-    cuuint64_t strides[2] = {pitch_bytes, depth_stride_bytes};
-    cuuint32_t box[3] = {box_inner, box_outer, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const cuuint64_t dims[3] = {inner, outer, depth};
+    const cuuint64_t strides[2] = {pitch_bytes, depth_stride_bytes};
+    const cuuint32_t box[3] = {box_inner, box_outer, 1};
+    return encode_cached(map, dtype, rank, base, dims, strides, box, swizzle,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 int launch_bf16_tcgen05(DeviceState *st, int M, int N, int K, float alpha, const uint16_t *A,

@@ -467,3 +467,42 @@ def test_sgemm_watchdog_reports_a_withheld_stage_and_recovers():
     g.sgemm(dA, dB, C)
     assert g.binding.get_device_status() == g.binding.GEMM_OK
     assert np.array_equal(C.cpu().numpy(), oracle.round_f32(oracle.gemm(A, B)))
+
+
+def test_tensor_map_reuse_across_calls_integer():
+    """Calls that repeat, or only partly repeat, an earlier call's base
+    addresses, shapes and pitches: the encoded tensor maps a call reuses must
+    match its own arguments exactly (more distinct operands than the
+    per-thread cache holds, the same buffers with a different M, N, pitch
+    or output type, and repeats)."""
+    M, N, K = 384, 520, 264
+    bufs = []
+    for i in range(10):
+        A = gi.draw("integer", 19000 + i, 0, (M, K), dtype="bf16")
+        B = gi.draw("integer", 19000 + i, 1, (K, N), dtype="bf16")
+        bufs.append((A, B, bf16_to_dev(A), bf16_to_dev(B)))
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    Cb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    for rnd in range(2):
+        for A, B, dA, dB in bufs:
+            g.gemm_bf16(dA, dB, C, out_dtype=torch.float32)
+            assert np.array_equal(C.cpu().numpy(), oracle.round_f32(oracle.gemm(A, B)))
+    A, B, dA, dB = bufs[0]
+    # same base addresses, fewer rows / columns (views), other pitches
+    g.gemm_bf16(dA[:200], dB, C[:200], out_dtype=torch.float32)
+    assert np.array_equal(C[:200].cpu().numpy(), oracle.round_f32(oracle.gemm(A[:200], B)))
+    sub = C[:, :256]
+    g.gemm_bf16(dA, dB[:, :256], sub, out_dtype=torch.float32)
+    assert np.array_equal(sub.cpu().numpy(), oracle.round_f32(oracle.gemm(A, B[:, :256])))
+    g.gemm_bf16(dA, dB, Cb)
+    assert np.array_equal(bf16_from_dev(Cb), oracle.round_bf16(oracle.gemm(A, B)))
+    # FP32 path through the same cache
+    Af = gi.draw("integer", 19100, 0, (M, K))
+    Bf = gi.draw("integer", 19100, 1, (K, N))
+    dAf, dBf = torch.from_numpy(Af).cuda(), torch.from_numpy(Bf).cuda()
+    for _ in range(2):
+        g.sgemm(dAf, dBf, C)
+        assert np.array_equal(C.cpu().numpy(), oracle.round_f32(oracle.gemm(Af, Bf)))
+    g.sgemm(dAf[:100], dBf, C[:100])
+    assert np.array_equal(C[:100].cpu().numpy(), oracle.round_f32(oracle.gemm(Af[:100], Bf)))
+    _status_ok()
