@@ -14,12 +14,14 @@
 //   * Persistent CTAs (one per SM), each walking output tiles
 //     (128 x BN, BN = 256 or 128) in grouped raster order.
 //   * Warp roles: warp 0 lane 0 issues TMA loads into an S-stage shared
-//     memory ring (A: one 64 x 128 box, K-major, 128-byte swizzle; B: BN/64
-//     boxes of 64 x 64, N-major, 128-byte swizzle); warp 1 allocates tensor
-//     memory and its lane 0 issues tcgen05.mma (M = 128, N = BN, K = 16)
-//     into one of two TMEM accumulators; warps 2-5 drain the other
-//     accumulator with tcgen05.ld, apply alpha/beta in fp32, convert and
-//     store, so a tile's epilogue overlaps the next tile's main loop.
+//     memory ring (A: the rows the launch needs, K-major, 128-byte swizzle;
+//     B: BN/64 boxes of 64 x 64, N-major, 128-byte swizzle; the stages are
+//     packed, so small-M launches get more of them); warp 1 allocates tensor
+//     memory and runs the MMA loop as a whole warp, one elected lane issuing
+//     each tcgen05.mma (M = 128, N = BN, K = 16) into one of two TMEM
+//     accumulators; warps 2-5 drain the other accumulator with tcgen05.ld,
+//     apply alpha/beta in fp32, convert and store, so a tile's epilogue
+//     overlaps the next tile's main loop.
 //   * Out-of-range rows/columns/K are zero-filled by TMA and masked at the
 //     store.
 //   * Split-K (small M x N): each (tile, K-slice) unit writes an fp32

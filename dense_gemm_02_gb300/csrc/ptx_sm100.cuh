@@ -122,29 +122,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *map, uint64_t
         : "memory");
 }
 
-// Same, with an L2 cache-policy hint (a createpolicy value).
-__device__ __forceinline__ void tma_load_2d_hint(void *dst, const void *map, uint64_t *bar,
-                                                 int c0, int c1, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1),
-        "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 // 2-D tiled bulk tensor copy shared -> global (a TMA store); rows and
 // columns outside the tensor are not written.  Completion is tracked with
 // bulk groups (commit / wait below).
@@ -223,27 +200,6 @@ __device__ __forceinline__ void tc_fence_before_sync() {
 
 __device__ __forceinline__ void tc_fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// D[tmem] (+)= A[smem desc] * B[smem desc], BF16 x BF16 -> FP32, one CTA.
-// accumulate == 0 overwrites D.
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrives once on `bar` when every tcgen05 operation this thread issued
-// before it has completed.
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_addr(bar))
-        : "memory");
 }
 
 // Each thread of the warp reads 32 consecutive 32-bit columns of its own TMEM
@@ -345,29 +301,6 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
-// D (both CTAs' TMEM, M = 256 split by rows) (+)= A (both CTAs' smem, 128
-// rows each) * B (both CTAs' smem, N/2 columns each).  Issued by one thread
-// of the even CTA; the descriptors name offsets valid in both CTAs.
-__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrives once on the mbarrier at `bar`'s offset in every CTA of cta_mask
-// when the pair MMAs issued so far by this thread have completed.
-__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_addr(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // Warp-uniform forms: every lane of a converged warp executes them and one
 // lane, chosen by elect.sync (the same lane each time while all 32 lanes
 // are active), issues the instruction.  Keeping the issuing loop
@@ -375,6 +308,8 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t cta_mas
 // issue back-to-back MMAs at the tensor pipe's rate: measured on GB300 with
 // a wait, a fence and a commit per four M = 256, N = 128 MMAs, 33 ns per
 // MMA against 49 ns from a single lane.
+// D[tmem] (+)= A[smem desc] * B[smem desc], BF16 x BF16 -> FP32, one CTA;
+// accumulate == 0 overwrites D.
 __device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -386,6 +321,8 @@ __device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
+// Arrives once on `bar` when every tcgen05 operation the elected lane
+// issued before it has completed.
 __device__ __forceinline__ void umma_commit_elect(uint64_t *bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
@@ -395,6 +332,9 @@ __device__ __forceinline__ void umma_commit_elect(uint64_t *bar) {
         : "memory");
 }
 
+// D (both CTAs' TMEM, M = 256 split by rows) (+)= A (both CTAs' smem, 128
+// rows each) * B (both CTAs' smem, N/2 columns each), issued from the even
+// CTA; the descriptors name offsets valid in both CTAs.
 __device__ __forceinline__ void umma_f16_pair_elect(uint32_t d_tmem, uint64_t a_desc,
                                                     uint64_t b_desc, uint32_t idesc,
                                                     uint32_t accumulate) {
@@ -407,6 +347,8 @@ __device__ __forceinline__ void umma_f16_pair_elect(uint32_t d_tmem, uint64_t a_
         : "memory");
 }
 
+// Arrives once on the mbarrier at `bar`'s offset in every CTA of cta_mask
+// when the pair MMAs the elected lane issued so far have completed.
 __device__ __forceinline__ void umma_commit_pair_elect(uint64_t *bar, uint16_t cta_mask) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
