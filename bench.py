@@ -27,6 +27,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -304,10 +305,16 @@ def config_block(workloads, args):
 
 
 def kernel_source_hash(w):
+    """Hash of the kernel's source code with comments and whitespace runs
+    removed, so that a comment edit keeps the recorded traffic valid and
+    any code edit invalidates it."""
     fname = "sgemm_tma.cu" if w.dtype == "f32" else "gemm_bf16_tc.cu"
     path = os.path.join(ROOT, "dense_gemm_02_gb300", "csrc", fname)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    with open(path, encoding="utf-8") as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256(" ".join(src.split()).encode()).hexdigest()[:16]
 
 
 def kernel_name(w):
