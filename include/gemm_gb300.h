@@ -45,8 +45,14 @@
  * synchronises the device) when a launch needs more than any before it on
  * that stream; gemm_shutdown() frees it.
  *
- * Thread safety: calls may come from several host threads; each call only
- * reads shared configuration.
+ * Thread safety: calls may come from several host threads.  Per-device
+ * state is created and grown under a lock.  A split-K workspace belongs to
+ * a stream, so calls that enqueue on the same stream from several threads
+ * at once must be ordered by the caller (as any work on one stream must
+ * be); gemm_shutdown() must not overlap other calls.  The host-buffer entry
+ * points run one at a time per process.  Encoded TMA descriptors are cached
+ * per thread.  The configuration knobs are process-wide and apply to calls
+ * that start after the change.
  */
 #ifndef GEMM_GB300_H
 #define GEMM_GB300_H
