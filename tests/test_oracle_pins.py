@@ -359,3 +359,48 @@ def test_fused_epilogue_order_bias_act_then_residual(oracle):
     # bf16 bias widens exactly
     bb = gi.f32_to_bf16_bits(bias.astype(np.float32))
     assert np.array_equal(oracle.gemm_fused(A, B, bias=bb), oracle.gemm_fused(A, B, bias=bias))
+
+
+# The tanh-form GELU the "Z-Turbo" page prints in its section 2.1,
+# 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), evaluated here in 40-digit
+# decimal arithmetic from nothing but that formula: pi from Machin's
+# arctangent series, tanh from exp.  These values tell the tanh form apart
+# from the erf form x * Phi(x) (at x = 1 they differ by 1.5e-4, at x = 2 by
+# 1e-4), which the identity and closeness pins above cannot.
+def _gelu_tanh_decimal(x):
+    from decimal import Decimal, localcontext
+
+    with localcontext() as ctx:
+        ctx.prec = 40
+
+        def atan_inv(n):  # arctan(1/n) by its Taylor series
+            n = Decimal(n)
+            term = total = 1 / n
+            k, sign, n2 = 1, -1, n * n
+            while True:
+                term /= n2
+                nxt = total + sign * term / (2 * k + 1)
+                if nxt == total:
+                    return total
+                total, k, sign = nxt, k + 1, -sign
+
+        pi = 16 * atan_inv(5) - 4 * atan_inv(239)
+        xd = Decimal(repr(float(x)))
+        u = (2 / pi).sqrt() * (xd + Decimal("0.044715") * xd ** 3)
+        e = (2 * u).exp()
+        return float(Decimal("0.5") * xd * (1 + (e - 1) / (e + 1)))
+
+
+def test_gelu_is_the_printed_tanh_form_not_the_erf_form(oracle):
+    xs = [1.0, 2.0, -1.0, -2.0, 0.5, 3.0, -0.25, 1.5]
+    got = oracle.act_values(xs, oracle.ACT_GELU)
+    for x, g in zip(xs, got):
+        want = _gelu_tanh_decimal(x)
+        assert abs(g - want) <= 1e-13 * max(1.0, abs(want)), (x, g, want)
+    # hand-checked values at 1 and 2 (tanh form), and the erf form's values,
+    # which must fail the comparison above
+    assert abs(_gelu_tanh_decimal(1.0) - 0.8411919906082768) < 1e-15
+    assert abs(_gelu_tanh_decimal(2.0) - 1.954597694087775) < 1e-14
+    for x, erf_form in [(1.0, 0.8413447460685429), (2.0, 1.9544997361036416)]:
+        assert abs(erf_form - 0.5 * x * (1 + math.erf(x / math.sqrt(2)))) < 1e-15
+        assert abs(erf_form - _gelu_tanh_decimal(x)) > 1e-5
