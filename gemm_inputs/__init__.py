@@ -38,6 +38,10 @@ for A, B and the input C, and seed + 0x100 for the integer-valued pass.
 
 from __future__ import annotations
 
+import os
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 __all__ = [
@@ -98,12 +102,42 @@ def splitmix64_stream(seed: int, stream: int, start: int, count: int) -> np.ndar
     return splitmix64_from_state(_stream_state(seed, stream), start, count)
 
 
+_pool = None
+_pool_lock = threading.Lock()
+
+
+def _threads() -> int:
+    try:
+        return max(1, min(32, len(os.sched_getaffinity(0))))
+    except AttributeError:  # pragma: no cover
+        return max(1, min(32, os.cpu_count() or 1))
+
+
+def _map_chunks(n: int, work) -> None:
+    """Runs work(lo, hi) over [0, n) in chunks of _CHUNK elements, on a
+    thread pool when there is more than one chunk.  Every element is a pure
+    function of its index, so the result does not depend on the split."""
+    spans = [(lo, min(n, lo + _CHUNK)) for lo in range(0, n, _CHUNK)]
+    if len(spans) <= 1:
+        for lo, hi in spans:
+            work(lo, hi)
+        return
+    global _pool
+    with _pool_lock:
+        if _pool is None:
+            _pool = ThreadPoolExecutor(max_workers=_threads())
+    for f in [_pool.submit(work, lo, hi) for lo, hi in spans]:
+        f.result()
+
+
 def _chunked(n: int, fn, offset: int = 0) -> np.ndarray:
     """fn(first_index, count) over [offset, offset + n) in chunks."""
     out = np.empty(n, dtype=np.float32)
-    for lo in range(0, n, _CHUNK):
-        hi = min(n, lo + _CHUNK)
+
+    def work(lo, hi):
         out[lo:hi] = fn(offset + lo, hi - lo)
+
+    _map_chunks(n, work)
     return out
 
 
@@ -151,13 +185,21 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     the rounding itself.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    lsb = (b >> np.uint64(16)) & np.uint64(1)
-    r = ((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
-    nan = np.isnan(x)
-    if nan.any():
-        r[nan] = ((b[nan] >> np.uint64(16)).astype(np.uint16) | np.uint16(0x0040))
-    return r
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint16)
+
+    def work(lo, hi):
+        xs = flat[lo:hi]
+        b = xs.view(np.uint32).astype(np.uint64)
+        lsb = (b >> np.uint64(16)) & np.uint64(1)
+        r = ((b + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+        nan = np.isnan(xs)
+        if nan.any():
+            r[nan] = ((b[nan] >> np.uint64(16)).astype(np.uint16) | np.uint16(0x0040))
+        out[lo:hi] = r
+
+    _map_chunks(flat.size, work)
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

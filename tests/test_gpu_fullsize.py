@@ -1,12 +1,16 @@
 """The five benchmark workloads at full size, launched exactly as the
 benchmark launches them (contiguous tensors through the tensor API), checked
-against the oracle on sampled outputs (the oracle computes those one by one)
-and, for the 256^3 case, on every output.
+against the oracle on EVERY output.
 
 Random pass: FP32 |C - C_ref| <= 1e-5 * K, BF16 |C - C_ref| <= 2^-7 |C_ref|
-+ 1e-2.  Integer pass ({-2..2} operands): sampled outputs bit-exact, and every
-output an integer multiple of alpha's granularity (a property that holds at
-any size).
++ 1e-2, elementwise.  Integer pass ({-2..2} operands, and C for the MLP
+shape): every output bit-exact against the oracle's double result rounded
+once to the output type.  The oracle is the multithreaded double triple
+loop; the largest workload (8192 x 14336 x 4096) takes about 20 s per pass
+on 16 host cores.
+
+C is pre-filled with NaN where beta = 0, so an output the kernel never wrote
+(or a read of C that should not happen) fails the comparison.
 """
 
 import numpy as np
@@ -20,8 +24,6 @@ from gpu_helpers import bf16_from_dev, bf16_to_dev, bf16_tolerance_violations, f
 
 pytestmark = pytest.mark.gpu
 
-N_SAMPLES = 3000
-
 
 @pytest.fixture(scope="module", autouse=True)
 def _built():
@@ -31,29 +33,20 @@ def _built():
     oracle.build()
 
 
-def sample_indices(M, N, seed):
-    r = np.random.default_rng(seed)
-    rows = r.integers(0, M, N_SAMPLES)
-    cols = r.integers(0, N, N_SAMPLES)
-    # corners and the last row/column (tile edges)
-    extra_r = np.array([0, 0, M - 1, M - 1] + [M - 1] * 16 + list(r.integers(0, M, 16)))
-    extra_c = np.array([0, N - 1, 0, N - 1] + list(r.integers(0, N, 16)) + [N - 1] * 16)
-    return np.concatenate([rows, extra_r]), np.concatenate([cols, extra_c])
-
-
 def run_workload(w, A, B, Cin):
+    out_dt = torch.bfloat16 if w.out == "bf16" else torch.float32
     if w.dtype == "f32":
         dA, dB = f32_to_dev(A), f32_to_dev(B)
-        dC = f32_to_dev(Cin) if Cin is not None else torch.empty((w.M, w.N), device="cuda")
+    else:
+        dA, dB = bf16_to_dev(A), bf16_to_dev(B)
+    if Cin is not None:
+        dC = bf16_to_dev(Cin) if w.out == "bf16" else f32_to_dev(Cin)
+    else:
+        dC = torch.full((w.M, w.N), float("nan"), device="cuda", dtype=out_dt)
+    if w.dtype == "f32":
         g.sgemm(dA, dB, dC, alpha=w.alpha, beta=w.beta)
         want = "sgemm_tma"
     else:
-        dA, dB = bf16_to_dev(A), bf16_to_dev(B)
-        if Cin is not None:
-            dC = bf16_to_dev(Cin) if w.out == "bf16" else f32_to_dev(Cin)
-        else:
-            dC = torch.empty((w.M, w.N), device="cuda",
-                             dtype=torch.bfloat16 if w.out == "bf16" else torch.float32)
         g.gemm_bf16(dA, dB, dC, alpha=w.alpha, beta=w.beta)
         want = "bf16_tcgen05"
     torch.cuda.synchronize()
@@ -65,36 +58,26 @@ def run_workload(w, A, B, Cin):
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
-def test_workload_random_pass(name):
+def test_workload_random_pass_every_output(name):
     w = WORKLOADS[name]
     A, B, Cin = w.operands()
     got = run_workload(w, A, B, Cin)
-    if w.M * w.N * w.K <= 256**3:
-        ref = oracle.gemm(A, B, Cin, alpha=w.alpha, beta=w.beta)
-        gv = widen(got, w.out)
-    else:
-        rows, cols = sample_indices(w.M, w.N, w.index)
-        ref = oracle.gemm_entries(A, B, rows, cols, Cin, alpha=w.alpha, beta=w.beta)
-        gv = widen(got[rows, cols], w.out)
-    assert np.isfinite(widen(got, w.out)).all()
+    ref = oracle.gemm(A, B, Cin, alpha=w.alpha, beta=w.beta)
+    gv = widen(got, w.out)
+    assert np.isfinite(gv).all()
     if w.dtype == "f32":
-        assert np.abs(gv - ref).max() <= 1e-5 * w.K
+        err = np.abs(gv - ref).max()
+        assert err <= 1e-5 * w.K, f"max |C - C_ref| = {err}"
     else:
         assert bf16_tolerance_violations(gv, ref) == 0
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
-def test_workload_integer_pass(name):
+def test_workload_integer_pass_bit_exact_everywhere(name):
     w = WORKLOADS[name]
     A, B, Cin = w.operands(integer=True)
     got = run_workload(w, A, B, Cin)
-    rows, cols = sample_indices(w.M, w.N, w.index + 100)
-    ref = oracle.gemm_entries(A, B, rows, cols, Cin, alpha=w.alpha, beta=w.beta)
-    if w.out == "bf16":
-        assert np.array_equal(got[rows, cols], oracle.round_bf16(ref))
-    else:
-        assert np.array_equal(got[rows, cols], oracle.round_f32(ref))
-    # every output is a multiple of alpha (integer sums times alpha) plus an
-    # integer C, so a multiple of 0.5 here
-    full = widen(got, w.out)
-    assert np.array_equal(full * 2, np.round(full * 2))
+    ref = oracle.gemm(A, B, Cin, alpha=w.alpha, beta=w.beta)
+    want = oracle.round_bf16(ref) if w.out == "bf16" else oracle.round_f32(ref)
+    diff = got != want
+    assert not diff.any(), f"{int(diff.sum())} of {diff.size} outputs differ"
