@@ -40,6 +40,8 @@ METRIC = "GEMM TFLOP/s (BF16 tcgen05, FP32 SIMT) at 4096^3 and % of chip peak"
 STEP_WORKLOADS = ("sgemm_4096", "bf16_4096")
 FLUSH_BYTES = 256 << 20
 WARM_REPS = 20  # back-to-back calls per kernel in the warm-L2 context pass
+# L2-flushed calls timed for each workload outside the headline step
+EXTRA_REPS = {"sgemm_256": 200, "bf16_mlp_8192x14336x4096": 20, "bf16_decode_64x8192x8192": 100}
 # Before each step the GPU idles this many cycles (~100 us) while the host
 # enqueues the step, so the host's launch overhead never shows up inside a
 # kernel's event window; the idle time is outside the timed events.
@@ -75,6 +77,13 @@ def parse_args():
                     help="override the workload's M, N, K (same distributions)")
     ap.add_argument("--config", action="append", default=[], metavar="KEY=VALUE",
                     help="library tuning knob (gemm_set_config), may repeat")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads (256^3, MLP and decode shapes) that the "
+                         "default step run also times and checks after its timed region")
+    ap.add_argument("--no-parity", action="store_true",
+                    help="skip the oracle comparison of the timed outputs")
+    ap.add_argument("--no-integer-pass", action="store_true",
+                    help="skip the bit-exact integer-operand pass of the parity check")
     return ap.parse_args()
 
 
@@ -211,11 +220,14 @@ def _sample_operands(w, rows, B_cache):
     return A, B_cache[w.name], C
 
 
-def oracle_sample_time(workloads, seconds_target):
+def oracle_sample_time(workloads, seconds_target, operands=None, keep=False):
     """Times the CPU oracle (all host threads) on the leading rows of each
     workload, with the row count chosen from a one-row-per-thread
-    calibration so the sample takes about seconds_target.
-    Returns (flops, seconds, rows, threads)."""
+    calibration so the sample takes about seconds_target (at most all M
+    rows).  `operands` maps a workload name to its full (A, B, C) host
+    arrays (else they are drawn here).  Returns (flops, seconds, rows,
+    threads, results); results maps each name to the oracle's double
+    product of those rows when `keep` is set."""
     import oracle
 
     oracle.build()
@@ -223,20 +235,91 @@ def oracle_sample_time(workloads, seconds_target):
     max_rows = min(w.M for w in workloads)
     B_cache = {}
 
+    def ops_for(rows):
+        out = []
+        for w in workloads:
+            if operands is not None and w.name in operands:
+                A, B, C = operands[w.name]
+                out.append((w, A[:rows], B, None if C is None else C[:rows]))
+            else:
+                out.append((w, *_sample_operands(w, rows, B_cache)))
+        return out
+
     def timed(rows):
-        ops = [(w, *_sample_operands(w, rows, B_cache)) for w in workloads]
+        ops = ops_for(rows)
+        res = {}
         t0 = time.perf_counter()
         for w, A, B, C in ops:
-            oracle.gemm(A, B, C, alpha=w.alpha, beta=w.beta, threads=threads)
-        return time.perf_counter() - t0
+            res[w.name] = oracle.gemm(A, B, C, alpha=w.alpha, beta=w.beta, threads=threads)
+        return time.perf_counter() - t0, res
 
     cal_rows = min(threads, max_rows)
-    t_cal = timed(cal_rows)
+    t_cal, res = timed(cal_rows)
     rows = int(cal_rows * seconds_target / max(t_cal, 1e-6))
     rows = max(cal_rows, min(max_rows, (rows // cal_rows) * cal_rows))
-    dt = timed(rows) if rows != cal_rows else t_cal
+    if rows != cal_rows:
+        dt, res = timed(rows)
+    else:
+        dt = t_cal
     flops = sum(2 * rows * w.N * w.K for w in workloads)
-    return flops, dt, rows, threads
+    return flops, dt, rows, threads, (res if keep else None)
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the
+    machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=20).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.machine() or "unknown"
+
+
+def parity_random(w, got, ref):
+    """Elementwise comparison of a GPU output (uint16 bf16 bits or float32)
+    with the oracle's double result under the workload's tolerance: FP32
+    |C - C_ref| <= 1e-5 K, BF16 |C - C_ref| <= 2^-7 |C_ref| + 1e-2."""
+    import numpy as np
+
+    import gemm_inputs as gi
+
+    gv = (gi.bf16_bits_to_f32(got) if w.out == "bf16" else got).astype(np.float64)
+    err = np.abs(gv - ref)
+    if w.dtype == "f32":
+        tol = np.full(1, 1e-5 * w.K)
+        tol_s = f"max|C - C_ref| <= 1e-5*K = {1e-5 * w.K:g}"
+    else:
+        tol = (2.0 ** -7) * np.abs(ref) + 1e-2
+        tol_s = "|C - C_ref| <= 2^-7 |C_ref| + 1e-2 elementwise"
+    bad = (err > tol) | ~np.isfinite(gv)
+    big = np.abs(ref) >= 1e-2  # relative error where the absolute floor does not dominate
+    rel = err[big] / np.abs(ref[big])
+    return {"compared": int(gv.size), "rows": int(gv.shape[0]),
+            "max_abs_err": float(np.max(err)) if err.size else 0.0,
+            "max_rel_err": float(np.max(rel)) if rel.size else 0.0,
+            "violations": int(bad.sum()), "tolerance": tol_s}
+
+
+def parity_integer(w, got, ref):
+    """Bit-exact comparison of a GPU output on {-2..2} operands with the
+    oracle's double result rounded once to the output type."""
+    import oracle
+
+    want = oracle.round_bf16(ref) if w.out == "bf16" else oracle.round_f32(ref)
+    return {"compared": int(got.size), "mismatches": int((got != want).sum()),
+            "rule": "bit-exact against the oracle rounded once to the output type"}
 
 
 def run_reference(args, dist):
@@ -251,7 +334,7 @@ def run_reference(args, dist):
     # steps (a minute by default), at least a few milliseconds per step
     per_step_target = max(0.005, min(60.0, 5.0 * args.cpu_seconds) /
                           max(1, args.steps + args.warmup))
-    _flops, _dt, rows, _threads = oracle_sample_time(workloads, per_step_target)
+    _flops, _dt, rows, _threads, _res = oracle_sample_time(workloads, per_step_target)
     B_cache = {}
     inputs = [(w, *_sample_operands(w, rows, B_cache)) for w in workloads]
 
@@ -390,8 +473,11 @@ def run_ours(args, dist):
     # ---- inputs resident in HBM
     dev_ops = []
     host_ops = []
+    host_np = {}  # name -> (A, B, C) host arrays of a single product, for the parity check
     for w in workloads:
         A, B, C = w.operands()
+        if nb == 1:
+            host_np[w.name] = (A, B, C)
         if nb > 1:  # matrices 0..nb-1 of a strided batch, stacked
             ops = [w.batch_operands(i) for i in range(nb)]
             A = np.stack([o[0] for o in ops])
@@ -461,7 +547,6 @@ def run_ours(args, dist):
     torch.cuda.synchronize()
     dist.barrier()
     wall = time.perf_counter() - t_wall0
-    clock_info = clocks.stop()
     g.binding.check(g.binding.get_device_status(), "timed-region device status")
 
     # Context only, outside the timed region: each kernel again, back to back
@@ -486,43 +571,99 @@ def run_ours(args, dist):
     value = dist.sum(flops_step * args.steps) / total_s / 1e12
     gpu_launches = nk * args.steps
 
-    sm_max = (clock_info or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz") or 2070.0
+    sm_max = peaks.get("sm_max_mhz") or 2070.0
     fp32_peak = sms * FP32_LANES_PER_SM * 2 * sm_max * 1e6 / 1e12
+
+    def roofline_of(w, ms, batch=1, traffic_ok=True):
+        tflops = w.flops * batch / (ms / 1e3) / 1e12
+        gbs = w.min_bytes() * batch / (ms / 1e3) / 1e9
+        traffic = recorded_traffic(w) if traffic_ok else None
+        if w.dtype == "f32":
+            return {"bound": "alu", "achieved": tflops, "peak": fp32_peak, "unit": "TFLOP/s",
+                    "frac": tflops / fp32_peak, "traffic": traffic,
+                    "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
+                                   f"x {sm_max:.0f} MHz (max SM clock)",
+                    "kernel": kernel_name(w)}
+        if w.M * w.N * w.K / (w.min_bytes() / 2) < 300:  # intensity below the ridge: HBM
+            peak_bw = peaks["hbm_gbs"]
+            return {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
+                    "frac": gbs / peak_bw, "traffic": traffic,
+                    "peak_source": f"{peak_src} hbm_gbs (of measured copy bandwidth)"
+                    if peak_src == "measured" else "fallback hbm_gbs",
+                    "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
+                    "kernel": kernel_name(w)}
+        pk = peaks["bf16_tflops"]
+        return {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s",
+                "frac": tflops / pk, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops (burst)",
+                "frac_of_sustained": tflops / peaks.get("bf16_tflops_sustained", pk),
+                "kernel": kernel_name(w)}
 
     kernels = {}
     rooflines = {}
     for i, w in enumerate(workloads):
         ms = statistics.mean(per_kernel_ms[i])
-        tflops = w.flops * nb / (ms / 1e3) / 1e12
-        gbs = w.min_bytes() * nb / (ms / 1e3) / 1e9
         warm = statistics.median(warm_ms[i])
-        entry = {"ms_mean": ms, "ms_median": statistics.median(per_kernel_ms[i]),
-                 "ms_min": min(per_kernel_ms[i]), "tflops": tflops, "min_bytes": w.min_bytes() * nb,
-                 "achieved_gbs_min_bytes": gbs,
-                 "warm_l2": {"ms_median": warm, "tflops": w.flops * nb / (warm / 1e3) / 1e12,
-                             "calls": WARM_REPS}}
-        if w.dtype == "f32":
-            rl = {"bound": "alu", "achieved": tflops, "peak": fp32_peak, "unit": "TFLOP/s",
-                  "frac": tflops / fp32_peak, "traffic": None if extended else recorded_traffic(w),
-                  "peak_source": f"derived: {sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 "
-                                 f"x {sm_max:.0f} MHz (max SM clock)",
-                  "kernel": kernel_name(w)}
-        elif w.M * w.N * w.K / (w.min_bytes() / 2) < 300:  # intensity below the ridge: HBM
-            peak_bw = peaks["hbm_gbs"]
-            rl = {"bound": "hbm", "achieved": gbs, "peak": peak_bw, "unit": "GB/s",
-                  "frac": gbs / peak_bw, "traffic": None if extended else recorded_traffic(w),
-                  "peak_source": f"{peak_src} hbm_gbs",
-                  "tensor_frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
-                  "kernel": kernel_name(w)}
-        else:
-            pk = peaks["bf16_tflops"]
-            rl = {"bound": "tensor", "achieved": tflops, "peak": pk, "unit": "TFLOP/s",
-                  "frac": tflops / pk, "traffic": None if extended else recorded_traffic(w),
-                  "peak_source": f"{peak_src} bf16_tflops (burst)",
-                  "frac_of_sustained": tflops / peaks.get("bf16_tflops_sustained", pk),
-                  "kernel": kernel_name(w)}
-        kernels[w.name] = entry
-        rooflines[w.name] = rl
+        kernels[w.name] = {
+            "ms_mean": ms, "ms_median": statistics.median(per_kernel_ms[i]),
+            "ms_min": min(per_kernel_ms[i]), "tflops": w.flops * nb / (ms / 1e3) / 1e12,
+            "min_bytes": w.min_bytes() * nb,
+            "achieved_gbs_min_bytes": w.min_bytes() * nb / (ms / 1e3) / 1e9,
+            "calls": args.steps, "timed": "inside the headline timed region",
+            "warm_l2": {"ms_median": warm, "tflops": w.flops * nb / (warm / 1e3) / 1e12,
+                        "calls": WARM_REPS}}
+        rooflines[w.name] = roofline_of(w, ms, nb, traffic_ok=not extended)
+
+    # ---- the other workloads (256^3, MLP and decode shapes): after the
+    # headline's timed region, each timed alone over a fixed number of
+    # L2-flushed calls, each with its own roofline; their outputs feed the
+    # parity check below.  Not part of `value`.
+    from gemm_inputs.workloads import WORKLOADS
+
+    run_extra = (args.workload == "step" and not extended and not args.shape
+                 and not args.no_extra and dist.rank == 0 and args.gpus == 1)
+    extra_outputs = {}
+    if run_extra:
+        for w in WORKLOADS.values():
+            if w.name in STEP_WORKLOADS:
+                continue
+            A, B, C = w.operands()
+            host_np[w.name] = (A, B, C)
+            dA, dB, dC, dC0 = _device_operands(torch, w, A, B, C)
+            op = (w, dA, dB, dC, None)
+            restore = (lambda dC=dC, dC0=dC0: dC.copy_(dC0)) if dC0 is not None else None
+            reps = EXTRA_REPS.get(w.name, 20)
+            for _ in range(3):
+                launch(*op)
+            torch.cuda.synchronize()
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(reps)]
+            for e0, e1 in evs:
+                if restore:
+                    restore()
+                torch.cuda._sleep(HOST_AHEAD_CYCLES)
+                flush.zero_()
+                e0.record(stream)
+                launch(*op)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            g.binding.check(g.binding.get_device_status(), f"{w.name} device status")
+            times = [e0.elapsed_time(e1) for e0, e1 in evs]
+            ms = statistics.mean(times)
+            kernels[w.name] = {
+                "ms_mean": ms, "ms_median": statistics.median(times), "ms_min": min(times),
+                "tflops": w.flops / (ms / 1e3) / 1e12, "min_bytes": w.min_bytes(),
+                "achieved_gbs_min_bytes": w.min_bytes() / (ms / 1e3) / 1e9, "calls": reps,
+                "timed": "after the headline timed region, alone, L2 flushed before each call"}
+            rooflines[w.name] = roofline_of(w, ms)
+            extra_outputs[w.name] = _host_output(torch, w, dC)  # C restored before the last call
+            del dA, dB, dC, dC0
+        torch.cuda.empty_cache()
+    clock_info = clocks.stop()
+    if clock_info is not None:
+        clock_info["window"] = ("timed region, then the warm-L2 pass and the other workloads' "
+                                "timed calls (GPU busy throughout)")
+
     dominant = max(range(nk), key=lambda i: statistics.mean(per_kernel_ms[i]))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
@@ -577,16 +718,130 @@ def run_ours(args, dist):
     else:
         line["e2e"] = None
 
-    # ---- CPU oracle baseline (rank 0, N = 1 only)
+    # ---- outputs of the timed launches, for the parity check: with
+    # beta == 0 every timed call wrote the same product; with beta != 0, C
+    # is restored and the product computed once more, as timed.
+    timed_outputs = {}
+    if nb == 1 and not extended and not args.no_parity and dist.rank == 0:
+        for (w, dA, dB, dC, bias), (_w, _hA, _hB, hC, _od) in zip(dev_ops, host_ops):
+            if w.beta != 0:
+                dC.copy_(hC.to(dC.device).view(dC.dtype))
+                launch(w, dA, dB, dC, bias)
+            timed_outputs[w.name] = _host_output(torch, w, dC)
+        timed_outputs.update(extra_outputs)
+        g.binding.check(g.binding.get_device_status(), "parity launch device status")
+
+    # ---- integer-operand pass ({-2..2}): one launch per workload on the
+    # same kernels, compared bit for bit below
+    int_outputs, int_inputs = {}, {}
+    if timed_outputs and not args.no_integer_pass:
+        for name in timed_outputs:
+            w = _workload_named(name, workloads)
+            A, B, C = w.operands(integer=True)
+            dA, dB, dC, _dC0 = _device_operands(torch, w, A, B, C)
+            launch(w, dA, dB, dC, None)
+            int_outputs[name] = _host_output(torch, w, dC)
+            int_inputs[name] = (A, B, C)
+            del dA, dB, dC, _dC0
+        g.binding.check(g.binding.get_device_status(), "integer pass device status")
+        torch.cuda.empty_cache()
+
+    # ---- CPU oracle (rank 0, N = 1 only): the baseline is the oracle timed
+    # on the headline workloads' own inputs (all host threads), and its
+    # products are the reference of the parity check.
     if dist.rank == 0 and args.gpus == 1 and not args.no_cpu_baseline:
-        flops, dt, rows, threads = oracle_sample_time(workloads, args.cpu_seconds)
+        import oracle
+
+        ops = {n: host_np[n] for n in host_np if n in [w.name for w in workloads]}
+        flops, dt, rows, threads, refs = oracle_sample_time(
+            workloads, args.cpu_seconds, operands=ops if nb == 1 else None, keep=True)
+        per = {}
         line["cpu_baseline"] = {
             "value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"leading {rows} rows of each of {', '.join(w.name for w in workloads)} "
-                      f"(full K and N), {dt:.1f} s on {threads} threads"}
+            "cpu_model": cpu_model(),
+            "sample": (f"leading {rows} of {min(w.M for w in workloads)} rows of each of "
+                       f"{', '.join(w.name for w in workloads)} (full K and N; the timed "
+                       f"run's own inputs), {dt:.1f} s on {threads} threads"),
+            "per_workload": per}
+        parity = {}
+        if timed_outputs:
+            for w in workloads:
+                if w.name in timed_outputs:
+                    parity[w.name] = {"random": parity_random(
+                        w, timed_outputs[w.name][:rows], refs[w.name])}
+            for name in extra_outputs:
+                w = WORKLOADS[name]
+                A, B, C = host_np[name]
+                t0 = time.perf_counter()
+                ref = oracle.gemm(A, B, C, alpha=w.alpha, beta=w.beta, threads=threads)
+                per[name] = {"all_cores_s": time.perf_counter() - t0, "threads": threads,
+                             "tflops": w.flops / (time.perf_counter() - t0) / 1e12}
+                parity[name] = {"random": parity_random(w, extra_outputs[name], ref)}
+                del ref
+            for name, got in int_outputs.items():
+                w = _workload_named(name, workloads)
+                A, B, C = int_inputs[name]
+                ref = oracle.gemm(A, B, C, alpha=w.alpha, beta=w.beta, threads=threads)
+                parity.setdefault(name, {})["integer"] = parity_integer(w, got, ref)
+                del ref
+            ok = all(v["random"]["violations"] == 0 and
+                     v.get("integer", {"mismatches": 0})["mismatches"] == 0
+                     for v in parity.values() if "random" in v)
+            line["parity"] = {"ok": ok, "oracle": "double-precision triple loop (oracle/)",
+                              "workloads": parity}
+        # the 256^3 case on one core and on all cores
+        w1 = WORKLOADS["sgemm_256"]
+        A, B, C = host_np.get(w1.name) or w1.operands()
+        for label, nt in (("one_core_s", 1), ("all_cores_s", threads)):
+            reps, t0 = 0, time.perf_counter()
+            while reps < 3 or time.perf_counter() - t0 < 0.5:
+                oracle.gemm(A, B, C, alpha=w1.alpha, beta=w1.beta, threads=nt)
+                reps += 1
+            per.setdefault(w1.name, {})[label] = (time.perf_counter() - t0) / reps
+        per[w1.name]["threads"] = threads
+    if "parity" not in line:
+        line["parity"] = None
     if dist.rank == 0:
         print(json.dumps(line))
     return 0
+
+
+def _workload_named(name, workloads):
+    from gemm_inputs.workloads import WORKLOADS
+
+    for w in workloads:
+        if w.name == name:
+            return w
+    return WORKLOADS[name]
+
+
+def _device_operands(torch, w, A, B, C):
+    """Device copies of one product's host operands (row-major, contiguous):
+    (A, B, C, pristine C or None).  C is NaN-filled when beta == 0, so an
+    output the kernel never writes cannot pass the parity check."""
+    out_dt = torch.float32 if w.out == "f32" else torch.bfloat16
+
+    def dev(x, kind):
+        if kind == "f32":
+            return torch.from_numpy(x).cuda()
+        return torch.from_numpy(x.view("int16")).cuda().view(torch.bfloat16)
+
+    dA, dB = dev(A, w.dtype), dev(B, w.dtype)
+    if C is not None:
+        dC0 = dev(C, w.out)
+        dC = dC0.clone()
+    else:
+        dC0 = None
+        dC = torch.full((w.M, w.N), float("nan"), dtype=out_dt, device="cuda")
+    return dA, dB, dC, dC0
+
+
+def _host_output(torch, w, dC):
+    """A device C as a host array: float32, or the uint16 bits of bf16."""
+    torch.cuda.synchronize()
+    if w.out == "f32":
+        return dC.cpu().numpy()
+    return dC.contiguous().view(torch.int16).cpu().numpy().view("uint16")
 
 
 def main():

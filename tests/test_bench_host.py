@@ -90,3 +90,48 @@ def test_peaks_table_has_the_denominators():
     peaks, source = bench.load_peaks()
     assert source in ("measured", "fallback")
     assert peaks["hbm_gbs"] > 0 and peaks["bf16_tflops"] > 0
+
+
+def test_parity_records_count_violations_and_mismatches(oracle):
+    import numpy as np
+
+    import gemm_inputs as gi
+
+    w32 = WORKLOADS["sgemm_256"]
+    ref = np.linspace(-3, 3, 12, dtype=np.float64).reshape(3, 4)
+    got = ref.astype(np.float32)
+    rec = bench.parity_random(w32, got, ref)
+    assert rec["violations"] == 0 and rec["compared"] == 12 and rec["rows"] == 3
+    got2 = got.copy()
+    got2[1, 2] += 1e-5 * w32.K * 2  # beyond 1e-5 K
+    got2[2, 3] = np.nan
+    assert bench.parity_random(w32, got2, ref)["violations"] == 2
+    # bf16 tolerance: 2^-7 |ref| + 1e-2, elementwise
+    wb = WORKLOADS["bf16_4096"]
+    refb = np.array([[100.0, -100.0, 0.0, 1.0]])
+    ok = gi.f32_to_bf16_bits(np.array([[100.5, -100.5, 0.009, 1.0]], np.float32))
+    assert bench.parity_random(wb, ok, refb)["violations"] == 0
+    bad = gi.f32_to_bf16_bits(np.array([[102.0, -100.0, 0.02, 1.0]], np.float32))
+    assert bench.parity_random(wb, bad, refb)["violations"] == 2
+    # integer pass: bit-exact after one rounding of the double result
+    refi = np.array([[3.0, -5.0, 257.0]])  # 257 rounds to 256 in bf16 (ties to even)
+    assert bench.parity_integer(wb, oracle.round_bf16(refi), refi)["mismatches"] == 0
+    off = oracle.round_bf16(refi)
+    off[0, 2] += 1
+    assert bench.parity_integer(wb, off, refi)["mismatches"] == 1
+
+
+def test_oracle_sample_keeps_products_of_given_operands(oracle):
+    import numpy as np
+
+    w = WORKLOADS["sgemm_256"]
+    A, B, C = w.operands()
+    flops, dt, rows, threads, res = bench.oracle_sample_time([w], 0.01, operands={w.name: (A, B, C)},
+                                                            keep=True)
+    assert rows >= 1 and flops == 2 * rows * w.N * w.K and dt > 0
+    assert np.array_equal(res[w.name], oracle.gemm(A[:rows], B, None))
+
+
+def test_cpu_model_is_a_name():
+    name = bench.cpu_model()
+    assert isinstance(name, str) and name

@@ -24,7 +24,7 @@ def run_bench(*args):
 
 
 def test_default_step_json_line():
-    d = run_bench("--steps", "3", "--warmup", "3", "--cpu-seconds", "2")
+    d = run_bench("--steps", "3", "--warmup", "3")
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
@@ -48,3 +48,19 @@ def test_default_step_json_line():
     assert e2e["value"] < d["value"]  # the copies are inside the end-to-end region
     assert d["clocks"]["sm_max_mhz"] > 0 and isinstance(d["clocks"]["reasons"], list)
     assert d["gpu_launches"] == 2 * 3  # one SGEMM and one BF16 launch per timed step
+    assert cb["cpu_model"] and cb["per_workload"]["sgemm_256"]["one_core_s"] > 0
+    # the timed outputs and the other workloads against the oracle
+    par = d["parity"]
+    assert par["ok"] is True
+    for name in ("sgemm_256", "sgemm_4096", "bf16_4096", "bf16_mlp_8192x14336x4096",
+                 "bf16_decode_64x8192x8192"):
+        rec = par["workloads"][name]
+        assert rec["random"]["violations"] == 0 and rec["random"]["compared"] > 0, name
+        assert rec["integer"]["mismatches"] == 0, name
+    # the headline products are compared whole (the oracle finishes 4096^3 in seconds)
+    assert par["workloads"]["bf16_4096"]["random"]["compared"] == 4096 * 4096
+    for name, bound in (("sgemm_256", "alu"), ("bf16_mlp_8192x14336x4096", "tensor"),
+                        ("bf16_decode_64x8192x8192", "hbm")):
+        rl = d["rooflines"][name]
+        assert rl["bound"] == bound and 0.0 < rl["frac"] < 1.5, name
+        assert d["kernels"][name]["calls"] > 0
