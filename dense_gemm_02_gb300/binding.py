@@ -60,6 +60,7 @@ SIGNATURES = {
     "gemm_f32_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64]),
     "gemm_bf16_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                               _int]),
+    "gemm_noalloc_get_status": (_int, [_vp, ctypes.POINTER(_i64)]),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_get_device_fault_info": (_i64, []),
     "gemm_status_string": (_cp, [_int]),
@@ -175,6 +176,14 @@ def gemm_f32_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:
 def gemm_bf16_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type) -> int:
     """Raw call of the host-buffer BF16 GEMM; A, B, C are host addresses."""
     return lib().gemm_bf16_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type)
+
+
+def noalloc_get_status(stream=None) -> tuple[int, int]:
+    """(status, fault info) of the allocation-free calls on the current
+    device; reading clears a recorded fault."""
+    info = ctypes.c_int64(0)
+    rc = lib().gemm_noalloc_get_status(stream, ctypes.byref(info))
+    return int(rc), int(info.value)
 
 
 def get_device_status(stream=None) -> int:

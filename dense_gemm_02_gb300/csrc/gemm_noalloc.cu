@@ -59,6 +59,14 @@ int scratch_for_current_device(int *device, ScratchSlot **out) {
             slot.status = GEMM_ERR_CUDA;
             return;
         }
+        // The fault record starts clear; afterwards only
+        // gemm_noalloc_get_status clears it, so a fault stays visible
+        // until the caller has asked.
+        if (cudaMemset(static_cast<unsigned char *>(ptr) + kFaultOffset, 0,
+                       sizeof(unsigned long long)) != cudaSuccess) {
+            slot.status = GEMM_ERR_CUDA;
+            return;
+        }
         slot.base = static_cast<unsigned char *>(ptr);
         slot.sm_count = sms;
         slot.status = GEMM_OK;
@@ -100,9 +108,26 @@ extern "C" int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
     ext.counters_n = kMaxTiles;
     ext.ws = reinterpret_cast<float *>(slot->base + kPartialsOffset);
     ext.ws_bytes = kScratchBytes - kPartialsOffset;
-    // The fault record starts clear for this call.
-    if (cudaMemsetAsync(ext.fault_word, 0, sizeof(unsigned long long), s) != cudaSuccess)
-        return GEMM_ERR_CUDA;
     return launch_bf16_tcgen05_external(device, slot->sm_count, ext, (int)M, (int)N, (int)K,
                                         alpha, A, lda, B, ldb, beta, C, ldc, c_f32, nullptr, s);
+}
+
+extern "C" int gemm_noalloc_get_status(void *stream, int64_t *fault_info) {
+    if (fault_info) *fault_info = 0;
+    int device = -1;
+    ScratchSlot *slot = nullptr;
+    int rc = scratch_for_current_device(&device, &slot);
+    if (rc != GEMM_OK) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    // An 8-byte read into the caller's stack and, if it held a fault, an
+    // 8-byte clear: plain copies, nothing allocated.
+    unsigned long long word = 0;
+    void *rec = slot->base + kFaultOffset;
+    if (cudaMemcpy(&word, rec, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (word == 0) return GEMM_OK;
+    if (fault_info) *fault_info = (int64_t)(word & ~kFaultFlag);
+    if (cudaMemset(rec, 0, sizeof(word)) != cudaSuccess) return GEMM_ERR_CUDA;
+    return GEMM_ERR_DEVICE_TIMEOUT;
 }

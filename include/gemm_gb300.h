@@ -247,13 +247,15 @@ GEMM_API int gemm_bf16_host(int64_t M, int64_t N, int64_t K, float alpha, const 
  *   - the first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first
  *     call before any stream capture on that device;
- *   - every call shares the one array and clears the parts that must start
- *     at zero (tile counters, fault record) on `stream` before its kernel;
+ *   - every call shares the one array and clears the part that must start
+ *     at zero (the split-K tile counters) on `stream` before its kernel;
  *     calls whose executions overlap on the GPU (different streams, no
  *     ordering between them) race on the array and give wrong results;
- *   - a pipeline wait that runs out of time is recorded only in the array's
- *     fault record (gemm_get_device_status does not see it); the kernel
- *     still returns and leaves this call's output incomplete.
+ *   - a pipeline wait that runs out of time is recorded in the array's
+ *     fault record, not in the status word gemm_get_device_status reads;
+ *     the kernel still returns and leaves that call's output incomplete.
+ *     The record keeps the first fault since it was last read:
+ *     gemm_noalloc_get_status below reports and clears it.
  * It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 #define GEMM_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -261,6 +263,20 @@ GEMM_API int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                                const uint16_t *A, int64_t lda, const uint16_t *B,
                                int64_t ldb, float beta, void *C, int64_t ldc, int c_type,
                                void *stream);
+
+/*
+ * Status of gemm_bf16_noalloc calls on the current device, for the same
+ * callers (it allocates nothing either; the source pages have no
+ * counterpart).  Synchronises `stream` (make it the stream, or the last of
+ * the streams, the calls ran on), reads the static array's fault record and
+ * returns GEMM_OK if no wait ran out since the record was last read, else
+ * GEMM_ERR_DEVICE_TIMEOUT and clears the record.  fault_info (may be NULL)
+ * receives the fault's details in the layout of
+ * gemm_get_device_fault_info, or 0.  GEMM_ERR_CUDA if a CUDA call failed.
+ * Like the first gemm_bf16_noalloc call, the first use on a device looks up
+ * the array's address and should come before any stream capture.
+ */
+GEMM_API int gemm_noalloc_get_status(void *stream, int64_t *fault_info);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's

@@ -1,13 +1,27 @@
-"""The allocation-free entry point, gemm_bf16_noalloc, for callers that
-cannot call cudaMalloc (code running under a host application that owns all
-device memory through its own allocator, or latency-critical code that
-cannot take an allocation's implicit synchronisation).  It runs the same
-tcgen05 kernel as gemm_bf16 but keeps its split-K scratch in a static device
-array inside the library.
+"""The allocation-free entry point, gemm_bf16_noalloc, and its status query.
 
-Checked through the C ABI against gemm_bf16 on two calls in a row, with the
-BF16 tolerance the other tests use (|C - C_ref| <= 2^-7 |C_ref| + 1e-2), and
-for its size limit.  This file is collected last on purpose.
+Some callers cannot call cudaMalloc at all: code running inside a host
+application whose device memory is entirely owned by that application's own
+arena or caching allocator (a plugin, a framework extension), or
+latency-critical code that cannot take the implicit synchronisation an
+allocation may cause.  For them the library offers a BF16 GEMM whose split-K
+scratch is a static device array compiled into the library, and
+gemm_noalloc_get_status, which reports a pipeline wait that ran out of time
+without allocating either.
+
+Checked through the C ABI:
+  * on two calls in a row, bit for bit against gemm_bf16 (the same kernel
+    with the same split choice), at shapes that split K;
+  * bit for bit against the oracle on integer operands (with the BF16
+    tolerance |C - C_ref| <= 2^-7 |C_ref| + 1e-2 on random operands);
+  * the device's free memory is unchanged across the calls (after a first
+    call has loaded the library's code and its static array);
+  * a withheld pipeline stage is reported by gemm_noalloc_get_status, which
+    then clears it, and the next call is correct;
+  * a split beyond the static scratch is refused before anything runs.
+
+This file is collected last on purpose, and every test in it works whether
+it runs alone in a fresh process or after the rest of the suite.
 """
 
 import numpy as np
@@ -15,6 +29,7 @@ import pytest
 import torch
 
 import gemm_inputs as gi
+import oracle
 from dense_gemm_02_gb300 import binding as b
 
 pytestmark = pytest.mark.gpu
@@ -25,6 +40,7 @@ def _built():
     from dense_gemm_02_gb300 import _build
 
     _build.build()
+    oracle.build()
     b.lib()
 
 
@@ -40,8 +56,25 @@ def _call(fn, A, B, C, alpha, beta):
               C.data_ptr(), C.stride(0), c_type, torch.cuda.current_stream().cuda_stream)
 
 
-def _as_f64(C):
-    return C.float().cpu().numpy().astype(np.float64)
+def _bits(C):
+    if C.dtype == torch.float32:
+        return C.cpu().numpy()
+    return C.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _operands(M, N, K, out, beta, seed, integer):
+    kind = "integer" if integer else "normal"
+    A = gi.draw(kind, seed, 0, (M, K), dtype="bf16")
+    B = gi.draw(kind, seed, 1, (K, N), sigma=0.02, dtype="bf16")
+    cdt = "bf16" if out == torch.bfloat16 else "f32"
+    C = gi.draw(kind, seed, 2, (M, N), dtype=cdt) if beta != 0.0 else None
+    return A, B, C
+
+
+def _dev_c(C, M, N, out):
+    if C is None:
+        return torch.full((M, N), float("nan"), device="cuda").to(out)
+    return _dev_bf16(C) if out == torch.bfloat16 else torch.from_numpy(C).cuda()
 
 
 # Small-M shapes, so that both entry points split K and the static scratch
@@ -52,24 +85,82 @@ CASES = [
 ]
 
 
-def test_noalloc_matches_gemm_bf16_on_two_calls_in_a_row():
+def test_noalloc_allocates_nothing_and_matches_gemm_bf16_bit_for_bit():
+    # every buffer this test uses exists before the measured calls
+    runs = []
     for call, (M, N, K, alpha, beta, out) in enumerate(CASES):
-        seed = 0x5EED0A00 + call
-        A = _dev_bf16(gi.draw("normal", seed, 0, (M, K), dtype="bf16"))
-        B = _dev_bf16(gi.draw("normal", seed, 1, (K, N), sigma=0.02, dtype="bf16"))
-        if beta != 0.0:
-            c0 = gi.draw("normal", seed, 2, (M, N), dtype="bf16" if out == torch.bfloat16 else "f32")
-            Cin = (_dev_bf16(c0) if out == torch.bfloat16 else torch.from_numpy(c0).cuda())
+        A, B, C = _operands(M, N, K, out, beta, 0x5EED0A00 + call, integer=False)
+        dA, dB = _dev_bf16(A), _dev_bf16(B)
+        Cin = _dev_c(C, M, N, out)
+        runs.append((dA, dB, Cin, Cin.clone(), Cin.clone(), alpha, beta))
+    warm = [r[2].clone() for r in runs]
+    torch.cuda.synchronize()
+    # A first call of each case loads the library's kernels and its static
+    # array (module loading is the driver's, not a call of ours); after that
+    # the device's free memory must not move.
+    for (dA, dB, _c, _r, _n, alpha, beta), Cw in zip(runs, warm):
+        assert _call(b.gemm_bf16_noalloc, dA, dB, Cw, alpha, beta) == b.GEMM_OK
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for dA, dB, _Cin, _C_ref, C_new, alpha, beta in runs:  # two calls in a row
+        assert _call(b.gemm_bf16_noalloc, dA, dB, C_new, alpha, beta) == b.GEMM_OK
+    assert b.noalloc_get_status(torch.cuda.current_stream().cuda_stream) == (b.GEMM_OK, 0)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    for dA, dB, _Cin, C_ref, C_new, alpha, beta in runs:
+        assert _call(b.gemm_bf16, dA, dB, C_ref, alpha, beta) == b.GEMM_OK
+    torch.cuda.synchronize()
+    for i, (_a, _b, _c, C_ref, C_new, _al, _be) in enumerate(runs):
+        got, want = _bits(C_new), _bits(C_ref)
+        assert np.array_equal(got, want), f"call {i}: differs from gemm_bf16"
+    for Cw, r in zip(warm, runs):  # the warm-up calls gave the same bits
+        assert np.array_equal(_bits(Cw), _bits(r[4]))
+
+
+@pytest.mark.parametrize("integer", [True, False], ids=["integer_bit_exact", "normal_tolerance"])
+def test_noalloc_matches_the_oracle(integer):
+    for call, (M, N, K, alpha, beta, out) in enumerate(CASES):
+        A, B, C = _operands(M, N, K, out, beta, 0x5EED0B00 + call, integer=integer)
+        dC = _dev_c(C, M, N, out)
+        assert _call(b.gemm_bf16_noalloc, _dev_bf16(A), _dev_bf16(B), dC, alpha, beta) == b.GEMM_OK
+        assert b.noalloc_get_status(torch.cuda.current_stream().cuda_stream)[0] == b.GEMM_OK
+        ref = oracle.gemm(A, B, C, alpha=alpha, beta=beta)
+        got = _bits(dC)
+        if integer:
+            want = oracle.round_bf16(ref) if out == torch.bfloat16 else oracle.round_f32(ref)
+            assert np.array_equal(got, want), f"call {call}"
         else:
-            Cin = torch.full((M, N), float("nan"), device="cuda").to(out)
-        C_ref, C_new = Cin.clone(), Cin.clone()
-        assert _call(b.gemm_bf16, A, B, C_ref, alpha, beta) == b.GEMM_OK
-        assert _call(b.gemm_bf16_noalloc, A, B, C_new, alpha, beta) == b.GEMM_OK
-        torch.cuda.synchronize()
-        ref, got = _as_f64(C_ref), _as_f64(C_new)
-        assert np.isfinite(got).all()
-        bad = np.abs(got - ref) > (2.0**-7) * np.abs(ref) + 1e-2
-        assert int(bad.sum()) == 0, f"call {call}: {int(bad.sum())} outputs out of tolerance"
+            gv = (gi.bf16_bits_to_f32(got) if out == torch.bfloat16 else got).astype(np.float64)
+            bad = (np.abs(gv - ref) > (2.0**-7) * np.abs(ref) + 1e-2) | ~np.isfinite(gv)
+            assert int(bad.sum()) == 0, f"call {call}: {int(bad.sum())} outputs out of tolerance"
+
+
+def test_noalloc_status_reports_a_withheld_stage_and_clears_it():
+    M, N, K = 64, 2048, 4096  # splits K
+    A = gi.draw("integer", 0x5EED0C00, 0, (M, K), dtype="bf16")
+    B = gi.draw("integer", 0x5EED0C00, 1, (K, N), dtype="bf16")
+    dA, dB = _dev_bf16(A), _dev_bf16(B)
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    assert b.noalloc_get_status(stream)[0] == b.GEMM_OK
+    old = b.get_config("watchdog_ms")
+    b.set_config("watchdog_ms", 200)
+    b.set_config("fault_inject", 1)  # the producer withholds one stage
+    try:
+        assert _call(b.gemm_bf16_noalloc, dA, dB, C, 1.0, 0.0) == b.GEMM_OK
+        rc, info = b.noalloc_get_status(stream)
+    finally:
+        b.set_config("fault_inject", 0)
+        b.set_config("watchdog_ms", old)
+    assert rc == b.GEMM_ERR_DEVICE_TIMEOUT
+    assert info & 0xFF in (1, 2, 3)  # producer, MMA issuer or epilogue
+    assert b.noalloc_get_status(stream) == (b.GEMM_OK, 0)  # read once, then clear
+    # the library's own status word is a different record
+    assert b.get_device_status(stream) == b.GEMM_OK
+    # the next call is correct
+    assert _call(b.gemm_bf16_noalloc, dA, dB, C, 1.0, 0.0) == b.GEMM_OK
+    assert b.noalloc_get_status(stream)[0] == b.GEMM_OK
+    assert np.array_equal(C.cpu().numpy(), oracle.round_f32(oracle.gemm(A, B)))
 
 
 def test_noalloc_rejects_a_split_beyond_its_scratch():
