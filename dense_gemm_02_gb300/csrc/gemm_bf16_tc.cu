@@ -1312,18 +1312,19 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
               TcParams &p, const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb,
               const GemmOpts &o, cudaStream_t stream) {
     using Cfg = TcCfg<BN>;
-    static bool attr_done[kMaxDevices] = {};
-    if (!attr_done[device]) {
-        const void *fns[4] = {(const void *)bf16_tc_kernel<BN, false, false>,
-                              (const void *)bf16_tc_kernel<BN, true, false>,
-                              (const void *)bf16_tc_kernel<BN, false, true>,
-                              (const void *)bf16_tc_kernel<BN, true, true>};
-        for (const void *fn : fns)
-            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     Cfg::SMEM_ALLOC) != cudaSuccess)
-                return GEMM_ERR_CUDA;
-        attr_done[device] = true;
-    }
+    static PerDeviceOnce attrs;
+    if (attrs.run(device, [] {
+            const void *fns[4] = {(const void *)bf16_tc_kernel<BN, false, false>,
+                                  (const void *)bf16_tc_kernel<BN, true, false>,
+                                  (const void *)bf16_tc_kernel<BN, false, true>,
+                                  (const void *)bf16_tc_kernel<BN, true, true>};
+            for (const void *fn : fns)
+                if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::SMEM_ALLOC) != cudaSuccess)
+                    return 1;
+            return 0;
+        }) != 0)
+        return GEMM_ERR_CUDA;
     alignas(64) CUtensorMap ta, tb, tc;
     if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb, o)) return GEMM_ERR_CUDA;
     if (!make_c_map(&tc, p, o.batch)) return GEMM_ERR_CUDA;
@@ -1458,11 +1459,25 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+cudaError_t query_resident_pairs(int *n);
+
 // Largest number of CTA pairs that can be resident at once.  A pair must sit
 // in one GPC, so this can be below sm_count / 2.
 int max_resident_pairs(int device) {
+    static PerDeviceOnce once;
     static int cache[kMaxDevices] = {};
-    if (cache[device] > 0) return cache[device];
+    if (once.run(device, [device] {
+            int n = 0;
+            if (query_resident_pairs(&n) != cudaSuccess || n <= 0) return 1;
+            cache[device] = n;
+            return 0;
+        }) != 0)
+        return 0;
+    return cache[device];
+}
+
+// Cluster occupancy of the CTA-pair kernel on the current device.
+cudaError_t query_resident_pairs(int *n) {
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(2048, 1, 1);
     lc.blockDim = dim3(TC_THREADS, 1, 1);
@@ -1474,29 +1489,25 @@ int max_resident_pairs(int device) {
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, bf16_tc2_kernel<false, false>, &lc) != cudaSuccess ||
-        n <= 0)
-        return 0;
-    cache[device] = n;
-    return n;
+    return cudaOccupancyMaxActiveClusters(n, bf16_tc2_kernel<false, false>, &lc);
 }
 
 int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const uint16_t *B,
                int64_t ldb, const GemmOpts &o, cudaStream_t stream) {
     using Cfg = Tc2Cfg;
-    static bool attr_done[kMaxDevices] = {};
-    if (!attr_done[device]) {
-        const void *fns[4] = {(const void *)bf16_tc2_kernel<false, false>,
-                              (const void *)bf16_tc2_kernel<true, false>,
-                              (const void *)bf16_tc2_kernel<false, true>,
-                              (const void *)bf16_tc2_kernel<true, true>};
-        for (const void *fn : fns)
-            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     Cfg::SMEM_ALLOC) != cudaSuccess)
-                return GEMM_ERR_CUDA;
-        attr_done[device] = true;
-    }
+    static PerDeviceOnce attrs;
+    if (attrs.run(device, [] {
+            const void *fns[4] = {(const void *)bf16_tc2_kernel<false, false>,
+                                  (const void *)bf16_tc2_kernel<true, false>,
+                                  (const void *)bf16_tc2_kernel<false, true>,
+                                  (const void *)bf16_tc2_kernel<true, true>};
+            for (const void *fn : fns)
+                if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg::SMEM_ALLOC) != cudaSuccess)
+                    return 1;
+            return 0;
+        }) != 0)
+        return GEMM_ERR_CUDA;
     const RuntimeConfig cfg = runtime_config();
     int pairs_max = max_resident_pairs(device);
     if (pairs_max <= 0) return GEMM_ERR_CUDA;

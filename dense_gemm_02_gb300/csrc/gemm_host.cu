@@ -104,41 +104,55 @@ int run_host(int64_t M, int64_t N, int64_t K, float alpha, const void *A, int64_
     const int64_t mb = round_up((M + nblk - 1) / nblk, 256);
     nblk = (M + mb - 1) / mb;
 
-    cudaEvent_t eB = hp->events[0];
-    if (reads_ab) {
-        if (!copy_rows(dB, ldb_d * ab_esz, B, ldb * ab_esz, N * ab_esz, K,
-                       cudaMemcpyHostToDevice, hp->in))
+    // Enqueues the whole pipeline; returns at the first failing call.
+    auto enqueue = [&]() -> int {
+        cudaEvent_t eB = hp->events[0];
+        if (reads_ab) {
+            if (!copy_rows(dB, ldb_d * ab_esz, B, ldb * ab_esz, N * ab_esz, K,
+                           cudaMemcpyHostToDevice, hp->in))
+                return GEMM_ERR_CUDA;
+        }
+        if (cudaEventRecord(eB, hp->in) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->compute, eB, 0) != cudaSuccess)
             return GEMM_ERR_CUDA;
-    }
-    if (cudaEventRecord(eB, hp->in) != cudaSuccess ||
-        cudaStreamWaitEvent(hp->compute, eB, 0) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    for (int64_t i = 0; i < nblk; ++i) {
-        const int64_t r0 = i * mb, m = std::min(mb, M - r0);
-        cudaEvent_t eIn = hp->events[1 + 2 * i], eOut = hp->events[2 + 2 * i];
-        if (reads_ab &&
-            !copy_rows(dA + r0 * lda_d * ab_esz, lda_d * ab_esz,
-                       static_cast<const char *>(A) + r0 * lda * ab_esz, lda * ab_esz,
-                       K * ab_esz, m, cudaMemcpyHostToDevice, hp->in))
-            return GEMM_ERR_CUDA;
-        if (beta != 0.f &&
-            !copy_rows(dC + r0 * ldc_d * c_esz, ldc_d * c_esz,
-                       static_cast<const char *>(C) + r0 * ldc * c_esz, ldc * c_esz, N * c_esz,
-                       m, cudaMemcpyHostToDevice, hp->in))
-            return GEMM_ERR_CUDA;
-        if (cudaEventRecord(eIn, hp->in) != cudaSuccess ||
-            cudaStreamWaitEvent(hp->compute, eIn, 0) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        rc = device_gemm(m, reads_ab ? dA + r0 * lda_d * ab_esz : nullptr, lda_d, dB, ldb_d,
-                         dC + r0 * ldc_d * c_esz, ldc_d, hp->compute);
-        if (rc != GEMM_OK) return rc;
-        if (cudaEventRecord(eOut, hp->compute) != cudaSuccess ||
-            cudaStreamWaitEvent(hp->out, eOut, 0) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        if (!copy_rows(static_cast<char *>(C) + r0 * ldc * c_esz, ldc * c_esz,
-                       dC + r0 * ldc_d * c_esz, ldc_d * c_esz, N * c_esz, m,
-                       cudaMemcpyDeviceToHost, hp->out))
-            return GEMM_ERR_CUDA;
+        for (int64_t i = 0; i < nblk; ++i) {
+            const int64_t r0 = i * mb, m = std::min(mb, M - r0);
+            cudaEvent_t eIn = hp->events[1 + 2 * i], eOut = hp->events[2 + 2 * i];
+            if (reads_ab &&
+                !copy_rows(dA + r0 * lda_d * ab_esz, lda_d * ab_esz,
+                           static_cast<const char *>(A) + r0 * lda * ab_esz, lda * ab_esz,
+                           K * ab_esz, m, cudaMemcpyHostToDevice, hp->in))
+                return GEMM_ERR_CUDA;
+            if (beta != 0.f &&
+                !copy_rows(dC + r0 * ldc_d * c_esz, ldc_d * c_esz,
+                           static_cast<const char *>(C) + r0 * ldc * c_esz, ldc * c_esz,
+                           N * c_esz, m, cudaMemcpyHostToDevice, hp->in))
+                return GEMM_ERR_CUDA;
+            if (cudaEventRecord(eIn, hp->in) != cudaSuccess ||
+                cudaStreamWaitEvent(hp->compute, eIn, 0) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            const int r = device_gemm(m, reads_ab ? dA + r0 * lda_d * ab_esz : nullptr, lda_d,
+                                      dB, ldb_d, dC + r0 * ldc_d * c_esz, ldc_d, hp->compute);
+            if (r != GEMM_OK) return r;
+            if (cudaEventRecord(eOut, hp->compute) != cudaSuccess ||
+                cudaStreamWaitEvent(hp->out, eOut, 0) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            if (!copy_rows(static_cast<char *>(C) + r0 * ldc * c_esz, ldc * c_esz,
+                           dC + r0 * ldc_d * c_esz, ldc_d * c_esz, N * c_esz, m,
+                           cudaMemcpyDeviceToHost, hp->out))
+                return GEMM_ERR_CUDA;
+        }
+        return GEMM_OK;
+    };
+    if ((rc = enqueue()) != GEMM_OK) {
+        // Copies and GEMMs of earlier blocks may still be running, some
+        // writing the caller's C: let them finish before the caller gets
+        // its buffers back.  Their own errors are not reported over rc.
+        cudaStreamSynchronize(hp->in);
+        cudaStreamSynchronize(hp->compute);
+        cudaStreamSynchronize(hp->out);
+        cudaGetLastError();
+        return rc;
     }
     if (cudaStreamSynchronize(hp->out) != cudaSuccess) return GEMM_ERR_CUDA;
     // A pipeline wait that ran out of time on the device shows here.

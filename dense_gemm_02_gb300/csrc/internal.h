@@ -5,8 +5,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <memory>
+#include <mutex>
 #include <vector>
 
 #include "gemm_gb300.h"
@@ -14,6 +16,28 @@
 namespace gemm {
 
 constexpr int kMaxDevices = 64;
+
+// One-time setup per device (function attributes, occupancy queries) that
+// several host threads may reach at once: the first caller on a device runs
+// `init` (0 = success) under a lock while the others wait; a failed setup
+// is tried again by the next call.  Returns init's result, or 0 once done.
+class PerDeviceOnce {
+  public:
+    template <class F>
+    int run(int device, F &&init) {
+        if (device < 0 || device >= kMaxDevices) return -1;
+        if (done_[device].load(std::memory_order_acquire)) return 0;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (done_[device].load(std::memory_order_relaxed)) return 0;
+        const int rc = init();
+        if (rc == 0) done_[device].store(true, std::memory_order_release);
+        return rc;
+    }
+
+  private:
+    std::mutex mu_;
+    std::atomic<bool> done_[kMaxDevices] = {};
+};
 
 // Device fault word layout (written once per fault by the first failing
 // thread with atomicCAS; 0 means no fault).

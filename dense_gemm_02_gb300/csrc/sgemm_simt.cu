@@ -213,17 +213,17 @@ __global__ void __launch_bounds__(THREADS, 2) sgemm_simt_kernel(const SimtParams
 template <bool VEC_B>
 cudaError_t launch_impl(const SimtParams &p, cudaStream_t stream) {
     // The shared-memory opt-in is a per-device function attribute.
-    static bool attr_done[kMaxDevices] = {};
+    static PerDeviceOnce attrs;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!attr_done[dev]) {
-        e = cudaFuncSetAttribute(sgemm_simt_kernel<VEC_B>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    if (attrs.run(dev, [&e] {
+            e = cudaFuncSetAttribute(sgemm_simt_kernel<VEC_B>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            return e == cudaSuccess ? 0 : 1;
+        }) != 0)
+        return e;
     const long long tiles = (long long)p.num_m_blk * p.num_n_blk;
     if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     sgemm_simt_kernel<VEC_B><<<(unsigned)tiles, THREADS, SMEM_BYTES, stream>>>(p);

@@ -290,13 +290,15 @@ __global__ void __launch_bounds__(TTHREADS, 2)
 int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const float *A,
                      int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,
                      const GemmOpts *opts, cudaStream_t stream) {
-    static bool attr_done[kMaxDevices] = {};
-    if (!attr_done[st->device]) {
-        if (cudaFuncSetAttribute(sgemm_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 TSMEM_ALLOC) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        attr_done[st->device] = true;
-    }
+    static PerDeviceOnce attrs;
+    if (attrs.run(st->device, [] {
+            return cudaFuncSetAttribute(sgemm_tma_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        TSMEM_ALLOC) == cudaSuccess
+                       ? 0
+                       : 1;
+        }) != 0)
+        return GEMM_ERR_CUDA;
     const GemmOpts o = opts ? *opts : GemmOpts{};
     const int64_t batch = o.batch > 1 ? o.batch : 1;
     alignas(64) CUtensorMap ta, tb;
