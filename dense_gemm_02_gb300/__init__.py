@@ -7,11 +7,11 @@ bias / activation epilogue.  This package is the thin Python binding.
 """
 
 from . import binding
-from .api import gemm, gemm_batched, gemm_bf16, gemm_ex, sgemm
+from .api import gemm, gemm_batched, gemm_bf16, gemm_ex, gemm_grouped, sgemm
 from .binding import GemmError, get_config, set_config
 
-__all__ = ["gemm", "gemm_batched", "gemm_bf16", "gemm_ex", "sgemm", "binding", "GemmError", "get_config",
-           "set_config", "flops"]
+__all__ = ["gemm", "gemm_batched", "gemm_bf16", "gemm_ex", "gemm_grouped", "sgemm", "binding",
+           "GemmError", "get_config", "set_config", "flops"]
 
 
 def flops(M: int, N: int, K: int) -> int:

@@ -4,7 +4,8 @@
 stride) and enqueue one library call on the current torch stream.
 ``gemm_ex`` adds transposed operands (a ``X.t()`` view is read in place)
 and the fused bias / activation epilogue; ``gemm_batched`` runs a strided
-batch of such products in one launch.
+batch of such products in one launch, ``gemm_grouped`` a list of problems of
+different shapes.
 ``gemm`` additionally accepts host (CPU) tensors, which it hands to the
 library's host-buffer entry points (copies pipelined with the computation):
 the end-to-end path of a caller holding host buffers.  Nothing here
@@ -121,6 +122,64 @@ def gemm_ex(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
                          _stream_handle(stream))
     _b.check(rc, "gemm_bf16_ex")
     return C
+
+
+def gemm_grouped(As, Bs, Cs=None, alphas=1.0, betas=0.0, out_dtype=None,
+                 stream=None) -> list:
+    """C_i = alpha_i * A_i @ B_i + beta_i * C_i for problems of different
+    shapes, in one library call (one launch per 64 problems).
+
+    As, Bs: sequences of CUDA tensors, all float32 (FP32 path) or all
+    bfloat16 (tensor cores); each A_i may be row-major or a transposed view
+    (``W.t()``), the same for every problem (likewise B_i).  Cs: None or a
+    sequence of C tensors (created when None; beta must then be 0).  alphas,
+    betas: a number or one per problem.  Returns the list of C tensors."""
+    As, Bs = list(As), list(Bs)
+    n = len(As)
+    if len(Bs) != n:
+        raise ValueError("As and Bs differ in length")
+    if n == 0:
+        return []
+    dt = As[0].dtype
+    if dt not in (torch.float32, torch.bfloat16) or any(t.dtype != dt for t in As + Bs):
+        raise TypeError("all operands must be float32, or all bfloat16")
+    if not all(t.is_cuda for t in As + Bs):
+        raise TypeError("operands must be CUDA tensors")
+    alphas = [float(alphas)] * n if isinstance(alphas, (int, float)) else [float(a) for a in alphas]
+    betas = [float(betas)] * n if isinstance(betas, (int, float)) else [float(b) for b in betas]
+    if len(alphas) != n or len(betas) != n:
+        raise ValueError("alphas and betas need one value per problem")
+    if dt == torch.float32:
+        out_dtype = torch.float32
+    elif out_dtype is None:
+        out_dtype = torch.bfloat16 if Cs is None else Cs[0].dtype
+    if Cs is None:
+        if any(b != 0.0 for b in betas):
+            raise ValueError("beta != 0 needs input Cs")
+        Cs = [torch.empty((a.shape[0], b.shape[1]), dtype=out_dtype, device=a.device)
+              for a, b in zip(As, Bs)]
+    Cs = list(Cs)
+    if len(Cs) != n or any(c.dtype != out_dtype or not c.is_cuda for c in Cs):
+        raise TypeError(f"Cs must be {n} CUDA tensors of {out_dtype}")
+    layouts = [(_layout(a, "A"), _layout(b, "B")) for a, b in zip(As, Bs)]
+    ta, tb = layouts[0][0][0], layouts[0][1][0]
+    if any(la[0] != ta or lb[0] != tb for la, lb in layouts):
+        raise ValueError("every A (and every B) must have the same layout")
+    problems = []
+    for (a, b, c, al, be, (la, lb)) in zip(As, Bs, Cs, alphas, betas, layouts):
+        M, N, K = _shapes(a, b, c)
+        problems.append((M, N, K, a.data_ptr(), la[1], b.data_ptr(), lb[1], c.data_ptr(),
+                         _row_major(c, "C"), al, be))
+    groups = _b.make_groups(problems)
+    opts = _b.make_opts(trans_a=ta, trans_b=tb)
+    if dt == torch.float32:
+        rc = _b.gemm_f32_grouped(groups, n, opts, _stream_handle(stream))
+        _b.check(rc, "gemm_f32_grouped")
+    else:
+        c_type = _b.GEMM_OUT_F32 if out_dtype == torch.float32 else _b.GEMM_OUT_BF16
+        rc = _b.gemm_bf16_grouped(groups, n, c_type, opts, _stream_handle(stream))
+        _b.check(rc, "gemm_bf16_grouped")
+    return Cs
 
 
 def gemm_batched(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,

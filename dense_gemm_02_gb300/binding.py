@@ -40,6 +40,15 @@ class GemmOpts(ctypes.Structure):
                 ("bias", ctypes.c_void_p), ("bias_type", ctypes.c_int),
                 ("act", ctypes.c_int)]
 
+class GemmGroup(ctypes.Structure):
+    """gemm_group_t: one problem of a grouped GEMM (device addresses)."""
+
+    _fields_ = [("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("A", ctypes.c_void_p), ("lda", ctypes.c_int64),
+                ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64),
+                ("C", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float)]
+
 # Every exported symbol of the C ABI, with (restype, argtypes).
 _i64, _f32, _vp, _int, _cp = (ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
                               ctypes.c_char_p)
@@ -57,6 +66,9 @@ SIGNATURES = {
                                  _f32, _vp, _i64, _i64, _int, ctypes.POINTER(GemmOpts), _vp]),
     "gemm_f32_batched": (_int, [_i64, _i64, _i64, _i64, _f32, _vp, _i64, _i64, _vp, _i64, _i64,
                                 _f32, _vp, _i64, _i64, ctypes.POINTER(GemmOpts), _vp]),
+    "gemm_bf16_grouped": (_int, [_i64, ctypes.POINTER(GemmGroup), _int, ctypes.POINTER(GemmOpts),
+                                 _vp]),
+    "gemm_f32_grouped": (_int, [_i64, ctypes.POINTER(GemmGroup), ctypes.POINTER(GemmOpts), _vp]),
     "gemm_f32_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64]),
     "gemm_bf16_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                               _int]),
@@ -166,6 +178,27 @@ def gemm_f32_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b, 
     ptr = ctypes.byref(opts) if opts is not None else None
     return lib().gemm_f32_batched(batch, M, N, K, alpha, A, lda, stride_a, B, ldb, stride_b,
                                   beta, C, ldc, stride_c, ptr, stream)
+
+
+def make_groups(problems) -> ctypes.Array:
+    """A gemm_group_t array from (M, N, K, A, lda, B, ldb, C, ldc, alpha,
+    beta) tuples (A, B, C device addresses)."""
+    arr = (GemmGroup * max(1, len(problems)))()
+    for i, pr in enumerate(problems):
+        arr[i] = GemmGroup(*pr)
+    return arr
+
+
+def gemm_bf16_grouped(groups, count, c_type, opts, stream) -> int:
+    """Raw call of the grouped BF16 GEMM; groups from make_groups."""
+    ptr = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_bf16_grouped(count, groups, c_type, ptr, stream)
+
+
+def gemm_f32_grouped(groups, count, opts, stream) -> int:
+    """Raw call of the grouped FP32 GEMM; groups from make_groups."""
+    ptr = ctypes.byref(opts) if opts is not None else None
+    return lib().gemm_f32_grouped(count, groups, ptr, stream)
 
 
 def gemm_f32_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:

@@ -4,10 +4,12 @@
 // this file only validates and launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "gemm_gb300.h"
 #include "internal.h"
@@ -342,10 +344,128 @@ int run_bf16(int64_t M, int64_t N, int64_t K, float alpha, const uint16_t *A, in
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Grouped GEMMs.  Every problem is checked as a single call would be; then
+// the problems, which run concurrently, must not write what another one
+// reads or writes: a C region may overlap no other region of the call
+// (operands that are only read, such as a weight matrix shared by several
+// problems, may overlap each other).  Checked by sorting the regions by
+// start address and sweeping once.
+int check_group_overlap(int64_t count, const gemm_group_t *g, const GemmOpts &o, size_t ab_esz,
+                        size_t c_esz) {
+    struct Region {
+        uintptr_t lo, hi;
+        bool write;
+    };
+    std::vector<Region> r;
+    r.reserve((size_t)count * 3);
+    for (int64_t i = 0; i < count; ++i) {
+        const gemm_group_t &x = g[i];
+        if (x.M == 0 || x.N == 0) continue;
+        const size_t cb = span_bytes(x.M, x.N, x.ldc, c_esz);
+        r.push_back({reinterpret_cast<uintptr_t>(x.C), reinterpret_cast<uintptr_t>(x.C) + cb, true});
+        if (x.alpha != 0.f && x.K > 0) {
+            const int64_t a_rows = o.trans_a ? x.K : x.M, a_cols = o.trans_a ? x.M : x.K;
+            const int64_t b_rows = o.trans_b ? x.N : x.K, b_cols = o.trans_b ? x.K : x.N;
+            const size_t ab = span_bytes(a_rows, a_cols, x.lda, ab_esz);
+            const size_t bb = span_bytes(b_rows, b_cols, x.ldb, ab_esz);
+            r.push_back({reinterpret_cast<uintptr_t>(x.A), reinterpret_cast<uintptr_t>(x.A) + ab,
+                         false});
+            r.push_back({reinterpret_cast<uintptr_t>(x.B), reinterpret_cast<uintptr_t>(x.B) + bb,
+                         false});
+        }
+    }
+    std::sort(r.begin(), r.end(), [](const Region &a, const Region &b) { return a.lo < b.lo; });
+    uintptr_t end_w = 0, end_any = 0;  // furthest end of earlier written / any regions
+    for (const Region &x : r) {
+        if (x.hi <= x.lo) continue;
+        if (x.lo < end_w || (x.write && x.lo < end_any)) return GEMM_ERR_ALIAS;
+        if (x.write) end_w = std::max(end_w, x.hi);
+        end_any = std::max(end_any, x.hi);
+    }
+    return GEMM_OK;
+}
+
+int run_grouped(bool bf16, int64_t count, const gemm_group_t *groups, int c_type,
+                const gemm_opts_t *opts, void *stream) {
+    GemmOpts o;
+    int rc = convert_opts(opts, &o);
+    if (rc != GEMM_OK) return rc;
+    if (has_epilogue(o)) return GEMM_ERR_INVALID_ARG;  // plain epilogue only
+    if (bf16 && c_type != GEMM_OUT_BF16 && c_type != GEMM_OUT_F32) return GEMM_ERR_INVALID_ARG;
+    if (count < 0) return GEMM_ERR_INVALID_ARG;
+    if (count > kMaxDim) return GEMM_ERR_TOO_LARGE;
+    if (count == 0) {
+        set_last_kernel("none");
+        return GEMM_OK;
+    }
+    if (!groups) return GEMM_ERR_NULLPTR;
+    const size_t ab_esz = bf16 ? 2 : 4;
+    const bool c_f32 = !bf16 || c_type == GEMM_OUT_F32;
+    const size_t c_esz = c_f32 ? 4 : 2;
+    for (int64_t i = 0; i < count; ++i) {
+        const gemm_group_t &x = groups[i];
+        rc = validate_gemm_args_ex(x.M, x.N, x.K, x.alpha, x.A, x.lda, ab_esz, o.trans_a, x.B,
+                                   x.ldb, ab_esz, o.trans_b, x.beta, x.C, x.ldc, c_esz);
+        if (rc != GEMM_OK && rc != 1) return rc;
+    }
+    if ((rc = check_group_overlap(count, groups, o, ab_esz, c_esz)) != GEMM_OK) return rc;
+    DeviceState *st = nullptr;
+    if ((rc = device_state(&st)) != GEMM_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool force_other = runtime_config().force_path == 1;
+    // Problems the grouped kernels take, and the rest one call at a time.
+    std::vector<GroupProblem> fast;
+    bool singles = false;  // some problem ran as a single call
+    for (int64_t i = 0; i < count; ++i) {
+        const gemm_group_t &x = groups[i];
+        if (x.M == 0 || x.N == 0) continue;
+        const bool tma = tma_operands_ok(o, x.M, x.N, x.K, x.A, x.lda, x.B, x.ldb, ab_esz);
+        const bool ok = x.alpha != 0.f && x.K > 0 && tma && !force_other &&
+                        (bf16 || (!o.trans_a && !o.trans_b));
+        if (ok) {
+            fast.push_back(GroupProblem{x.M, x.N, x.K, x.A, x.lda, x.B, x.ldb, x.C, x.ldc,
+                                        x.alpha, x.beta});
+            continue;
+        }
+        rc = bf16 ? run_bf16(x.M, x.N, x.K, x.alpha, static_cast<const uint16_t *>(x.A), x.lda,
+                             static_cast<const uint16_t *>(x.B), x.ldb, x.beta, x.C, x.ldc,
+                             c_type, o, stream)
+                  : run_f32(x.M, x.N, x.K, x.alpha, static_cast<const float *>(x.A), x.lda,
+                            static_cast<const float *>(x.B), x.ldb, x.beta,
+                            static_cast<float *>(x.C), x.ldc, o, stream);
+        if (rc != GEMM_OK) return rc;
+        singles = true;
+    }
+    for (size_t i0 = 0; i0 < fast.size(); i0 += kMaxGroupsPerLaunch) {
+        const int n = (int)std::min<size_t>(kMaxGroupsPerLaunch, fast.size() - i0);
+        rc = bf16 ? launch_bf16_tcgen05_grouped(st, n, fast.data() + i0, c_f32, o.trans_a,
+                                                o.trans_b, s)
+                  : launch_sgemm_tma_grouped(st, n, fast.data() + i0, s);
+        if (rc != GEMM_OK) return rc;
+    }
+    if (singles && !fast.empty())
+        set_last_kernel(bf16 ? "bf16_grouped_mixed" : "f32_grouped_mixed");
+    else if (!fast.empty())
+        set_last_kernel(bf16 ? "bf16_tcgen05_grouped" : "sgemm_tma_grouped");
+    else if (!singles)
+        set_last_kernel("none");
+    return GEMM_OK;
+}
+
 }  // namespace
 }  // namespace gemm
 
 using namespace gemm;
+
+extern "C" int gemm_bf16_grouped(int64_t count, const gemm_group_t *groups, int c_type,
+                                 const gemm_opts_t *opts, void *stream) {
+    return run_grouped(true, count, groups, c_type, opts, stream);
+}
+
+extern "C" int gemm_f32_grouped(int64_t count, const gemm_group_t *groups,
+                                const gemm_opts_t *opts, void *stream) {
+    return run_grouped(false, count, groups, GEMM_OUT_F32, opts, stream);
+}
 
 extern "C" int gemm_f32(int64_t M, int64_t N, int64_t K, float alpha, const float *A,
                         int64_t lda, const float *B, int64_t ldb, float beta, float *C,

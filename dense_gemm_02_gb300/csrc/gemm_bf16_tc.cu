@@ -263,10 +263,16 @@ __device__ __forceinline__ bool cta_unit(const TcParams &p, int i, Unit &w) {
     return true;
 }
 
+__device__ __forceinline__ void record_fault_word(unsigned long long *fault_word,
+                                                  volatile int *abort_flag, unsigned role,
+                                                  unsigned stage, unsigned tile) {
+    *abort_flag = 1;
+    atomicCAS(fault_word, 0ull, fault_code(role, stage, tile));
+}
+
 __device__ __forceinline__ void record_fault(const TcParams &p, volatile int *abort_flag,
                                              unsigned role, unsigned stage, unsigned tile) {
-    *abort_flag = 1;
-    atomicCAS(p.fault_word, 0ull, fault_code(role, stage, tile));
+    record_fault_word(p.fault_word, abort_flag, role, stage, tile);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
@@ -1172,6 +1178,267 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
 }
 
+// ================================================================ grouped
+//
+// One persistent launch over the output tiles of up to kMaxGroupsPerLaunch
+// problems of different shapes and operands (the grouped GEMM that
+// "Blackwell BF16 GEMM ..." (lshu.cn), section 3.1, lists among a GEMM
+// library's capabilities).  Tile u of the launch belongs to the last
+// problem whose first tile is <= u; within a problem, 128 x 256 tiles in
+// grouped raster order.  Warp roles, ring, TMEM double buffering and the
+// epilogue are those of the single-CTA kernel (whole tiles only: no split
+// and no narrower tail tiles); every problem's A, B and C tensor maps travel
+// in the kernel parameters.
+struct BgGroup {
+    int M, N, num_m_blk, num_n_blk, num_kb, tile0;
+    float alpha, beta;
+    void *C;
+    long long ldc;
+    int c_vec, c_tma;
+};
+struct BgParams {
+    CUtensorMap ma[kMaxGroupsPerLaunch];
+    CUtensorMap mb[kMaxGroupsPerLaunch];
+    CUtensorMap mc[kMaxGroupsPerLaunch];
+    BgGroup g[kMaxGroupsPerLaunch];
+    int groups, units, c_f32;
+    int stages, stage_bytes;
+    unsigned long long *fault_word;
+    unsigned long long timeout_ns;
+    int fault_inject;
+};
+constexpr int kGroupedBN = 256;
+
+// Problem of launch tile u (problems have at least one tile each, so their
+// first tiles increase strictly), and the tile's block coordinates in it.
+__device__ __forceinline__ int group_tile(const BgParams &p, int u, int &m_blk, int &n_blk) {
+    int g = 0;
+    for (int i = 1; i < p.groups; ++i)
+        if (p.g[i].tile0 <= u) g = i;
+    const BgGroup &d = p.g[g];
+    grouped_tile_coords(u - d.tile0, d.num_m_blk, d.num_n_blk, kRasterGroup, m_blk, n_blk);
+    return g;
+}
+
+template <bool A_MN, bool B_KM>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    bf16_tc_grouped_kernel(const __grid_constant__ BgParams p) {
+    constexpr int BN = kGroupedBN;
+    using Cfg = TcCfg<BN>;
+    constexpr int SMAX = Cfg::MAX_STAGES;
+    const uint32_t S = (uint32_t)p.stages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t *ring = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + SMAX;
+    uint64_t *tfull = bars + 2 * SMAX;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
+    uint32_t *tmem_slot = misc;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 1);
+    volatile int *epi_ok = reinterpret_cast<volatile int *>(misc + 3);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int a_slot = Cfg::A_BYTES;  // 128 rows of A per stage, in either layout
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], TC_EPI_THREADS);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *epi_ok = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t tx = (uint32_t)a_slot + (BN / 64) * Cfg::B_BOX_BYTES;
+            uint32_t it = 0, s = 0, ph = 0;
+            int withheld = -1;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+                int m_blk, n_blk;
+                const int g = group_tile(p, u, m_blk, n_blk);
+                const int m0 = m_blk * TC_BM, n0 = n_blk * BN;
+                const int nkb = p.g[g].num_kb;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t cur = s, cur_ph = ph;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                    if (!mbar_wait(&empty[cur], cur_ph ^ 1u, abort_flag, p.timeout_ns)) {
+                        record_fault_word(p.fault_word, abort_flag, kRoleProducer, cur, u);
+                        ok = false;
+                        break;
+                    }
+                    if (p.fault_inject && blockIdx.x == 0 && it == 0) {
+                        withheld = 0;  // test hook: this stage is never filled
+                        continue;
+                    }
+                    mbar_arrive_expect_tx(&full[cur], tx);
+                    uint8_t *a_dst = ring + cur * (uint32_t)p.stage_bytes;
+                    uint8_t *b_dst = a_dst + a_slot;
+                    const int k0 = kb * TC_BK;
+                    if constexpr (A_MN) {
+                        tma_load_2d(a_dst, &p.ma[g], &full[cur], m0, k0);
+                        tma_load_2d(a_dst + 8192, &p.ma[g], &full[cur], m0 + 64, k0);
+                    } else {
+                        tma_load_2d(a_dst, &p.ma[g], &full[cur], k0, m0);
+                    }
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j) {
+                        if constexpr (B_KM)
+                            tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &p.mb[g], &full[cur], k0,
+                                        n0 + j * 64);
+                        else
+                            tma_load_2d(b_dst + j * Cfg::B_BOX_BYTES, &p.mb[g], &full[cur],
+                                        n0 + j * 64, k0);
+                    }
+                }
+            }
+            // Let every copy started here land before the CTA can exit.
+            const uint32_t first = it > S ? it - S : 0u;
+            for (uint32_t i = first; i < it; ++i) {
+                if ((int)i == withheld) continue;
+                mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (whole warp)
+        const OperandLayout la = operand_layout(A_MN), lb = operand_layout(!B_KM);
+        const uint64_t a_desc0 = smem_desc_sw128(smem_addr(ring), la.lbo, 1024);
+        const uint64_t b_desc0 = smem_desc_sw128(smem_addr(ring + a_slot), lb.lbo, 1024);
+        const uint32_t stage_bytes = (uint32_t)p.stage_bytes;
+        const uint32_t a1 = la.step, a2 = 2 * la.step, a3 = 3 * la.step;
+        const uint32_t b1 = lb.step, b2 = 2 * lb.step, b3 = 3 * lb.step;
+        const uint32_t idesc = idesc_bf16_f32(BN, TC_BM, A_MN, B_KM);
+        uint32_t s = 0, ph = 0, local = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+            int m_blk, n_blk;
+            const int g = group_tile(p, u, m_blk, n_blk);
+            const int nkb = p.g[g].num_kb;
+            const uint32_t b = local & 1u, use = local >> 1;
+            ++local;
+            const bool got = mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, p.timeout_ns);
+            if (__any_sync(0xffffffffu, !got)) {
+                if (lane == 0) record_fault_word(p.fault_word, abort_flag, kRoleMma, 0xfe, u);
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t d_tmem = tmem_base + b * BN;
+            uint32_t acc = 0;
+            for (int kb = 0; kb < nkb; ++kb) {
+                const bool ready = mbar_wait(&full[s], ph, abort_flag, p.timeout_ns);
+                if (__any_sync(0xffffffffu, !ready)) {
+                    if (lane == 0) record_fault_word(p.fault_word, abort_flag, kRoleMma, s, u);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint64_t ad = desc_add(a_desc0, s * stage_bytes);
+                const uint64_t bd = desc_add(b_desc0, s * stage_bytes);
+                umma_f16_elect(d_tmem, ad, bd, idesc, acc);
+                umma_f16_elect(d_tmem, ad + a1, bd + b1, idesc, 1u);
+                umma_f16_elect(d_tmem, ad + a2, bd + b2, idesc, 1u);
+                umma_f16_elect(d_tmem, ad + a3, bd + b3, idesc, 1u);
+                umma_commit_elect(&empty[s]);  // frees the stage once these MMAs finish
+                acc = 1u;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            umma_commit_elect(&tfull[b]);  // accumulator b is complete
+        }
+        // The elected lane's MMAs must finish before TMEM is released.
+        umma_commit_elect(drain);
+        mbar_wait(drain, 0, abort_flag, p.timeout_ns, true);
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ epilogue warps 2-5
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        const int et = threadIdx.x - 64;
+        uint8_t *warp_stage = smem + Cfg::OFF_STAGE + q * 2 * kEpiChunkBytes;
+        uint32_t stage_seq = 0;
+        uint32_t local = 0;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            int m_blk, n_blk;
+            const int g = group_tile(p, u, m_blk, n_blk);
+            const BgGroup &d = p.g[g];
+            const uint32_t b = local & 1u, use = local >> 1;
+            ++local;
+            if (et == 0) {
+                const bool ok = mbar_wait(&tfull[b], use & 1u, abort_flag, p.timeout_ns);
+                if (!ok) record_fault_word(p.fault_word, abort_flag, kRoleEpilogue, 0xff, u);
+                *epi_ok = ok ? 1 : 0;
+            }
+            named_bar_sync(TC_EPI_BAR, TC_EPI_THREADS);
+            if (!*epi_ok) break;
+            mbar_wait(&tfull[b], use & 1u, abort_flag, p.timeout_ns, true);  // completed: no wait
+            tc_fence_after_sync();
+            // The store helpers read these fields of a parameter block.
+            TcParams tp{};
+            tp.M = d.M;
+            tp.N = d.N;
+            tp.ldc = d.ldc;
+            tp.beta = d.beta;
+            tp.c_f32 = p.c_f32;
+            tp.c_vec = d.c_vec;
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + b * BN;
+            const int gm = m_blk * TC_BM + row;
+            const int gn0 = n_blk * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tbase + c * 32, r);
+                tmem_ld_wait();
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if (d.c_tma)
+                    store_chunk_tma<false>(tp, d.alpha, d.C, 0, &p.mc[g], warp_stage, stage_seq,
+                                           lane, gm - lane, gn0 + c * 32, v);
+                else
+                    store_row_chunk(tp, d.alpha, d.C, gm, gn0 + c * 32, v);
+            }
+            tc_fence_before_sync();
+            mbar_arrive(&tempty[b]);
+        }
+    }
+
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // TMA stores of C have landed
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1581,6 +1848,85 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Grouped launch: the A, B and C tensor maps of each problem as the
+// single-CTA kernel would encode them (128-row A boxes, 256-column tiles).
+template <bool A_MN, bool B_KM>
+int launch_grouped_layout(int device, int sm_count, BgParams &gp, cudaStream_t stream) {
+    using Cfg = TcCfg<kGroupedBN>;
+    static PerDeviceOnce attrs;
+    if (attrs.run(device, [] {
+            return cudaFuncSetAttribute(bf16_tc_grouped_kernel<A_MN, B_KM>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        Cfg::SMEM_ALLOC) == cudaSuccess
+                       ? 0
+                       : 1;
+        }) != 0)
+        return GEMM_ERR_CUDA;
+    const int grid = gp.units < sm_count ? gp.units : sm_count;
+    bf16_tc_grouped_kernel<A_MN, B_KM><<<grid, TC_THREADS, Cfg::SMEM_ALLOC, stream>>>(gp);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+int launch_grouped(int device, int sm_count, unsigned long long *fault_word, int count,
+                   const GroupProblem *g, bool c_f32, int trans_a, int trans_b,
+                   cudaStream_t stream) {
+    using Cfg = TcCfg<kGroupedBN>;
+    if (count < 1 || count > kMaxGroupsPerLaunch) return GEMM_ERR_INVALID_ARG;
+    static_assert(sizeof(BgParams) <= 32000, "kernel parameter space");
+    thread_local BgParams gp;  // about 28 KiB: kept off the stack
+    long long tiles = 0;
+    GemmOpts o{};
+    o.trans_a = trans_a;
+    o.trans_b = trans_b;
+    for (int i = 0; i < count; ++i) {
+        const GroupProblem &x = g[i];
+        TcParams tp{};
+        tp.M = (int)x.M;
+        tp.N = (int)x.N;
+        tp.K = (int)x.K;
+        tp.a_mn = trans_a ? 1 : 0;
+        tp.b_kmaj = trans_b ? 1 : 0;
+        tp.a_rows = TC_BM;
+        tp.C = x.C;
+        tp.ldc = x.ldc;
+        tp.c_f32 = c_f32 ? 1 : 0;
+        if (!make_ab_maps(&gp.ma[i], &gp.mb[i], tp, static_cast<const uint16_t *>(x.A), x.lda,
+                          static_cast<const uint16_t *>(x.B), x.ldb, o) ||
+            !make_c_map(&gp.mc[i], tp, 1))
+            return GEMM_ERR_CUDA;
+        BgGroup &d = gp.g[i];
+        d.M = tp.M;
+        d.N = tp.N;
+        d.num_m_blk = (tp.M + TC_BM - 1) / TC_BM;
+        d.num_n_blk = (tp.N + kGroupedBN - 1) / kGroupedBN;
+        d.num_kb = (tp.K + TC_BK - 1) / TC_BK;
+        d.tile0 = (int)tiles;
+        d.alpha = x.alpha;
+        d.beta = x.beta;
+        d.C = x.C;
+        d.ldc = x.ldc;
+        const int esz = c_f32 ? 4 : 2;
+        d.c_vec = ((reinterpret_cast<uintptr_t>(x.C) & 15) == 0) && ((x.ldc * esz) % 16 == 0);
+        d.c_tma = tp.c_tma;
+        tiles += (long long)d.num_m_blk * d.num_n_blk;
+        if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    }
+    gp.groups = count;
+    gp.units = (int)tiles;
+    gp.c_f32 = c_f32 ? 1 : 0;
+    gp.stage_bytes = Cfg::A_BYTES + Cfg::B_BYTES;
+    gp.stages = std::min(Cfg::MAX_STAGES, Cfg::RING_BYTES / gp.stage_bytes);
+    gp.fault_word = fault_word;
+    const RuntimeConfig cfg = runtime_config();
+    gp.timeout_ns = (unsigned long long)cfg.watchdog_ms * 1000000ull;
+    gp.fault_inject = cfg.fault_inject ? 1 : 0;
+    if (gp.fault_inject) consume_fault_inject();
+    if (!trans_a && !trans_b) return launch_grouped_layout<false, false>(device, sm_count, gp, stream);
+    if (!trans_a) return launch_grouped_layout<false, true>(device, sm_count, gp, stream);
+    if (!trans_b) return launch_grouped_layout<true, false>(device, sm_count, gp, stream);
+    return launch_grouped_layout<true, true>(device, sm_count, gp, stream);
+}
+
 }  // namespace
 
 namespace {
@@ -1679,6 +2025,12 @@ int launch_bf16_tcgen05_external(int device, int sm_count, const ExternalScratch
                                  cudaStream_t stream) {
     return launch_common(device, sm_count, nullptr, &ext, ext.fault_word, M, N, K, alpha, A, lda,
                          B, ldb, beta, C, ldc, c_f32, opts, stream);
+}
+
+int launch_bf16_tcgen05_grouped(DeviceState *st, int count, const GroupProblem *g, bool c_f32,
+                                int trans_a, int trans_b, cudaStream_t stream) {
+    return launch_grouped(st->device, st->sm_count, st->fault_word, count, g, c_f32, trans_a,
+                          trans_b, stream);
 }
 
 }  // namespace gemm

@@ -196,6 +196,35 @@ int validate_gemm_args_ex(int64_t M, int64_t N, int64_t K, float alpha, const vo
                           size_t b_esz, bool trans_b, float beta, const void *C, int64_t ldc,
                           size_t c_esz);
 
+// One problem of a grouped GEMM (host side): C = alpha * op(A) * op(B) +
+// beta * C with its own sizes, pointers and pitches (elements).
+struct GroupProblem {
+    int64_t M, N, K;
+    const void *A;
+    int64_t lda;
+    const void *B;
+    int64_t ldb;
+    void *C;
+    int64_t ldc;
+    float alpha, beta;
+};
+// Groups one grouped launch can carry: their tensor maps and sizes travel in
+// the kernel's parameters (up to 32 KiB), not in a device buffer.
+constexpr int kMaxGroupsPerLaunch = 64;
+
+// Grouped FP32 SGEMM on the TMA kernel: one launch over every tile of
+// `count` (<= kMaxGroupsPerLaunch) problems, all with 16-byte aligned A/B
+// bases, lda and ldb multiples of 4, M, N, K > 0 and alpha != 0.  Returns a
+// gemm_status_t.
+int launch_sgemm_tma_grouped(DeviceState *st, int count, const GroupProblem *g,
+                             cudaStream_t stream);
+// Grouped BF16 tcgen05 GEMM: one persistent launch over the union of the
+// problems' output tiles, in the layouts trans_a / trans_b select (shared by
+// all problems); the same preconditions with 16-byte aligned pitches (in
+// elements: multiples of 8).  Returns a gemm_status_t.
+int launch_bf16_tcgen05_grouped(DeviceState *st, int count, const GroupProblem *g, bool c_f32,
+                                int trans_a, int trans_b, cudaStream_t stream);
+
 // Split-K storage supplied by the caller instead of the library workspace.
 struct ExternalScratch {
     float *ws;                       // fp32 partial tiles

@@ -71,9 +71,13 @@ struct TmaParams {
     unsigned *counters;  // one per split tile
 };
 
-__global__ void __launch_bounds__(TTHREADS, 2)
-    sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const TmaParams p) {
+// The work of one CTA: output tile (m_blk, n_blk) of matrix bidx of the
+// batch, whole (slice < 0) or one K slice of split tile `tile`.  The plain
+// and the grouped kernels both run it (force-inlined, so each compiles to
+// its own straight-line kernel).
+__device__ __forceinline__ void sgemm_cta(const CUtensorMap *tmA, const CUtensorMap *tmB,
+                                          const TmaParams &p, int tile, int slice, int m_blk,
+                                          int n_blk, int bidx) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + TOFF_BAR);
@@ -84,19 +88,6 @@ __global__ void __launch_bounds__(TTHREADS, 2)
     const int warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 2, wn = warp & 3;  // 2 x 4 warps, warp tile 64 x 32
     const int tm = lane >> 2, tn = lane & 3;  // 8 x 4 threads, thread tile 8 x 8
-
-    // Blocks 0..tiles_main-1 compute whole tiles; each later block one K
-    // slice of a tile of the partial last wave.
-    int tile = blockIdx.x, slice = -1;
-    if (tile >= p.tiles_main) {
-        const int v = tile - p.tiles_main;
-        tile = p.tiles_main + v / p.splits;
-        slice = v - (v / p.splits) * p.splits;
-    }
-    const int bidx = tile / p.tiles_per_batch;
-    int m_blk, n_blk;
-    grouped_tile_coords(tile - bidx * p.tiles_per_batch, p.num_m_blk, p.num_n_blk, kRasterGroup,
-                        m_blk, n_blk);
     const int m0 = m_blk * TBM, n0 = n_blk * TBN;
     const int ab = bidx * p.a_bmul, bb = bidx * p.b_bmul;  // TMA batch coordinates
     const int KT_all = (p.K + TBK - 1) / TBK;
@@ -107,8 +98,8 @@ __global__ void __launch_bounds__(TTHREADS, 2)
         for (int s = 0; s < TSTAGES; ++s) mbar_init(&full[s], 1);
         *never = 0;
         fence_barrier_init();
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+        prefetch_tensormap(tmA);
+        prefetch_tensormap(tmB);
     }
     __syncthreads();
 
@@ -116,8 +107,8 @@ __global__ void __launch_bounds__(TTHREADS, 2)
         const int s = kt % TSTAGES;
         uint8_t *st = smem + s * TSTAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], TSTAGE_BYTES);
-        tma_load_3d(st, &tmA, &full[s], (kt0 + kt) * TBK, m0, ab);
-        tma_load_3d(st + TA_BYTES, &tmB, &full[s], n0, (kt0 + kt) * TBK, bb);
+        tma_load_3d(st, tmA, &full[s], (kt0 + kt) * TBK, m0, ab);
+        tma_load_3d(st + TA_BYTES, tmB, &full[s], n0, (kt0 + kt) * TBK, bb);
     };
     int issued = 0;
     if (tid == 0)
@@ -285,7 +276,107 @@ __global__ void __launch_bounds__(TTHREADS, 2)
     }
 }
 
+__global__ void __launch_bounds__(TTHREADS, 2)
+    sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const TmaParams p) {
+    // Blocks 0..tiles_main-1 compute whole tiles; each later block one K
+    // slice of a tile of the partial last wave.
+    int tile = blockIdx.x, slice = -1;
+    if (tile >= p.tiles_main) {
+        const int v = tile - p.tiles_main;
+        tile = p.tiles_main + v / p.splits;
+        slice = v - (v / p.splits) * p.splits;
+    }
+    const int bidx = tile / p.tiles_per_batch;
+    int m_blk, n_blk;
+    grouped_tile_coords(tile - bidx * p.tiles_per_batch, p.num_m_blk, p.num_n_blk, kRasterGroup,
+                        m_blk, n_blk);
+    sgemm_cta(&tmA, &tmB, p, tile, slice, m_blk, n_blk, bidx);
+}
+
+// Grouped GEMM: problem g owns launch tiles tile0[g] .. tile0[g+1] - 1; its
+// A and B tensor maps and its whole parameter block travel in the kernel
+// parameters (read from there where they are used, not held in registers).
+struct SgGroupedParams {
+    CUtensorMap ma[kMaxGroupsPerLaunch];
+    CUtensorMap mb[kMaxGroupsPerLaunch];
+    TmaParams tp[kMaxGroupsPerLaunch];
+    int tile0[kMaxGroupsPerLaunch];
+    int groups;
+};
+
+__global__ void __launch_bounds__(TTHREADS, 2)
+    sgemm_tma_grouped_kernel(const __grid_constant__ SgGroupedParams gp) {
+    // The problem of this block: the last one whose first tile is <= it
+    // (every problem has at least one tile, so tile0 increases strictly).
+    int g = 0;
+    for (int i = 1; i < gp.groups; ++i)
+        if (gp.tile0[i] <= (int)blockIdx.x) g = i;
+    const TmaParams &q = gp.tp[g];
+    const int t = (int)blockIdx.x - gp.tile0[g];
+    int m_blk, n_blk;
+    grouped_tile_coords(t, q.num_m_blk, q.num_n_blk, kRasterGroup, m_blk, n_blk);
+    sgemm_cta(&gp.ma[g], &gp.mb[g], q, t, -1, m_blk, n_blk, 0);
+}
+
 }  // namespace
+
+int launch_sgemm_tma_grouped(DeviceState *st, int count, const GroupProblem *g,
+                             cudaStream_t stream) {
+    static PerDeviceOnce attrs;
+    if (attrs.run(st->device, [] {
+            return cudaFuncSetAttribute(sgemm_tma_grouped_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        TSMEM_ALLOC) == cudaSuccess
+                       ? 0
+                       : 1;
+        }) != 0)
+        return GEMM_ERR_CUDA;
+    if (count < 1 || count > kMaxGroupsPerLaunch) return GEMM_ERR_INVALID_ARG;
+    static_assert(sizeof(SgGroupedParams) <= 32000, "kernel parameter space");
+    // The parameter block is large; it lives on the heap of this thread.
+    thread_local SgGroupedParams gp;
+    long long tiles = 0;
+    for (int i = 0; i < count; ++i) {
+        const GroupProblem &x = g[i];
+        if (!encode_tensor_map_3d(&gp.ma[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.A, (uint64_t)x.K,
+                                  (uint64_t)x.M, 1, (uint64_t)x.lda * 4, 0, TBK, TBM,
+                                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_tensor_map_3d(&gp.mb[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x.B, (uint64_t)x.N,
+                                  (uint64_t)x.K, 1, (uint64_t)x.ldb * 4, 0, TBN, TBK,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GEMM_ERR_CUDA;
+        TmaParams &q = gp.tp[i];
+        q = TmaParams{};
+        q.M = (int)x.M;
+        q.N = (int)x.N;
+        q.K = (int)x.K;
+        q.alpha = x.alpha;
+        q.beta = x.beta;
+        q.C = static_cast<float *>(x.C);
+        q.ldc = x.ldc;
+        q.c_vec = ((reinterpret_cast<uintptr_t>(x.C) & 15) == 0) && (x.ldc % 4 == 0);
+        q.num_m_blk = (q.M + TBM - 1) / TBM;
+        q.num_n_blk = (q.N + TBN - 1) / TBN;
+        q.tiles_main = 0x7fffffff;  // whole tiles only
+        q.splits = 1;
+        q.tiles_per_batch = 0x7fffffff;
+        gp.tile0[i] = (int)tiles;
+        tiles += (long long)q.num_m_blk * q.num_n_blk;
+        if (tiles > 0x7fffffffLL) return GEMM_ERR_TOO_LARGE;
+    }
+    gp.groups = count;
+    const RuntimeConfig cfg = runtime_config();
+    const int inject = cfg.fault_inject ? 1 : 0;
+    if (inject) consume_fault_inject();
+    for (int i = 0; i < count; ++i) {
+        gp.tp[i].fault_word = st->fault_word;
+        gp.tp[i].timeout_ns = (unsigned long long)cfg.watchdog_ms * 1000000ull;
+        gp.tp[i].fault_inject = inject;
+    }
+    sgemm_tma_grouped_kernel<<<(unsigned)tiles, TTHREADS, TSMEM_ALLOC, stream>>>(gp);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
 
 int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const float *A,
                      int64_t lda, const float *B, int64_t ldb, float beta, float *C, int64_t ldc,

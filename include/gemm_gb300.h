@@ -205,6 +205,49 @@ GEMM_API int gemm_f32_batched(int64_t batch, int64_t M, int64_t N, int64_t K, fl
                               int64_t stride_c, const gemm_opts_t *opts, void *stream);
 
 /*
+ * One problem of a grouped GEMM: C = alpha * op(A) * op(B) + beta * C with
+ * its own sizes, operands, pitches (elements) and scalars.  A and B are bf16
+ * (uint16 bits) for gemm_bf16_grouped and fp32 for gemm_f32_grouped; C has
+ * the call's output type.
+ */
+typedef struct {
+    int64_t M, N, K;
+    const void *A;
+    int64_t lda;
+    const void *B;
+    int64_t ldb;
+    void *C;
+    int64_t ldc;
+    float alpha, beta;
+} gemm_group_t;
+
+/*
+ * Grouped GEMMs: `count` problems of different shapes and operands in one
+ * call ("Blackwell BF16 GEMM ..." (lshu.cn), section 3.1, lists grouped
+ * GEMM among the capabilities of a GEMM library).  groups is a HOST array of
+ * count gemm_group_t (read during the call only).  Each problem follows the
+ * rules of gemm_bf16 / gemm_f32 (pitches, NULL pointers, beta == 0 leaves C
+ * unread, alpha == 0 or K == 0 gives beta * C, empty problems do nothing);
+ * opts may select transposed layouts (trans_a / trans_b apply to every
+ * problem) but no bias or activation (GEMM_ERR_INVALID_ARG).  Because the
+ * problems run concurrently, no problem's C may overlap any other
+ * problem's A, B or C, and none its own A or B (GEMM_ERR_ALIAS); A and B
+ * may be shared between problems.
+ * Problems whose operands TMA can fetch (16-byte aligned bases, pitches in
+ * multiples of 16 bytes; FP32 also row-major) run in ONE persistent launch
+ * per 64 problems over the union of their output tiles (the tcgen05 kernel
+ * for bf16, the TMA SGEMM for fp32); the others run one call each.
+ * The grouped launch never splits K; results meet the same tolerances as
+ * the single calls (and on integer-valued inputs are exact either way).
+ * Returns GEMM_OK or a gemm_status_t error; argument errors are reported
+ * before anything is launched.
+ */
+GEMM_API int gemm_bf16_grouped(int64_t count, const gemm_group_t *groups, int c_type,
+                               const gemm_opts_t *opts, void *stream);
+GEMM_API int gemm_f32_grouped(int64_t count, const gemm_group_t *groups,
+                              const gemm_opts_t *opts, void *stream);
+
+/*
  * Host-buffer GEMMs: the same products with A, B and C in HOST memory
  * (pinned memory gives the full copy bandwidth; pageable memory works).  The
  * library copies B and then A (and C when beta != 0) to the device in row
@@ -328,6 +371,8 @@ GEMM_API int gemm_get_config(const char *key, int64_t *value);
 /*
  * Name of the kernel the last successful gemm_* call on this host thread
  * launched ("sgemm_tma", "sgemm_simt", "bf16_tcgen05", "bf16_simt", "scale_c",
+ * "sgemm_tma_grouped", "bf16_tcgen05_grouped", "bf16_grouped_mixed" or
+ * "f32_grouped_mixed" (a grouped call that also ran single calls),
  * "none").
  */
 GEMM_API const char *gemm_last_kernel(void);

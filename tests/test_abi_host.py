@@ -195,3 +195,38 @@ def test_ctypes_signatures_match_header_arity(lib):
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(params) == len(args), name
     assert isinstance(lib, ctypes.CDLL)
+
+
+def test_grouped_entry_point_errors(lib):
+    """gemm_bf16_grouped / gemm_f32_grouped: every problem's checks and the
+    cross-problem overlap check run before any CUDA call."""
+    from dense_gemm_02_gb300 import binding as b
+
+    fake = 1 << 24
+
+    def prob(A, B, C, M=4, N=4, K=4, lda=4, ldb=4, ldc=4, alpha=1.0, beta=0.0):
+        return (M, N, K, A, lda, B, ldb, C, ldc, alpha, beta)
+
+    for grouped, esz in ((lambda g, n, o=None: b.gemm_bf16_grouped(g, n, b.GEMM_OUT_F32, o, None), 2),
+                         (lambda g, n, o=None: b.gemm_f32_grouped(g, n, o, None), 4)):
+        A0, B0, C0 = fake, fake + 4096, fake + 8192
+        A1, B1, C1 = fake + 12288, fake + 16384, fake + 20480
+        ok = [prob(A0, B0, C0), prob(A1, B1, C1)]
+        assert grouped(b.make_groups([]), -1) == b.GEMM_ERR_INVALID_ARG
+        assert grouped(None, 0) == b.GEMM_OK  # nothing to do
+        assert grouped(None, 2) == b.GEMM_ERR_NULLPTR
+        # a bad pitch in the second problem
+        assert grouped(b.make_groups([ok[0], prob(A1, B1, C1, lda=2)]), 2) == b.GEMM_ERR_BAD_LD
+        # a missing operand
+        assert grouped(b.make_groups([ok[0], prob(None, B1, C1)]), 2) == b.GEMM_ERR_NULLPTR
+        # no epilogue in grouped calls
+        assert grouped(b.make_groups(ok), 2, b.make_opts(act=b.GEMM_ACT_RELU)) == \
+            b.GEMM_ERR_INVALID_ARG
+        # problem 1 writes into problem 0's A, B or C
+        for target in (A0, B0, C0 + 8):
+            bad = [ok[0], prob(A1, B1, target)]
+            assert grouped(b.make_groups(bad), 2) == b.GEMM_ERR_ALIAS, target
+        # problem 1 reads problem 0's C
+        assert grouped(b.make_groups([ok[0], prob(C0, B1, C1)]), 2) == b.GEMM_ERR_ALIAS
+        # (shared read-only operands are allowed: tested on the GPU with
+        # real buffers, since a call that passes the checks launches)
