@@ -6,9 +6,14 @@ input: the FP32 SGEMM 4096^3 (CUDA cores) followed by the BF16 GEMM 4096^3
 (tcgen05 tensor cores, fp32 accumulate, bf16 out).  `--workload` selects a
 single workload instead (see gemm_inputs/workloads.py).
 
-Timing: W untimed warm-up steps, then K timed steps.  Before every step a
-256 MiB buffer is written to flush the 129 MB L2 (outside the timed events);
-each kernel is bracketed by CUDA events on the stream it is launched on.
+Timing: W untimed warm-up steps, then K timed steps.  Before every step the
+129 MB L2 is flushed, outside the timed events: a 256 MiB buffer is written
+(evicting every line), then a second 256 MiB buffer is read, so that the
+dirty lines the write leaves are written back before the step instead of
+during it (measured on GB300: left dirty, their write-back slows a
+bandwidth-bound kernel by 5-7 us, a cost of the flush, not of the kernel;
+the workloads timed after the step also report the write-only flush).
+Each kernel is bracketed by CUDA events on the stream it is launched on.
 `value` = work of all ranks / the slowest rank's summed step time.  Prints
 one JSON line (rank 0).  For context, after the timed region each kernel
 also runs back to back without the flush (`kernels.*.warm_l2`).
@@ -377,7 +382,8 @@ def config_block(workloads, args):
                             "alpha": w.alpha, "beta": w.beta, "dist": w.description}
                    for w in workloads},
         "layout": "row-major A (MxK), B (KxN), C (MxN), contiguous",
-        "l2": "flushed before every step by writing a 256 MiB buffer (outside the timed events)",
+        "l2": ("flushed before every step (outside the timed events): a 256 MiB buffer written, "
+               "then a second 256 MiB buffer read, so no dirty line is left to write back"),
         "host_ahead": "the GPU idles ~100 us before each step (outside the timed events) so "
                       "kernel events exclude host launch overhead",
         "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU",
@@ -509,7 +515,13 @@ def run_ours(args, dist):
         host_ops.append((w, hA.pin_memory(), hB.pin_memory(),
                          hC.pin_memory() if hC is not None else None, out_dt))
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+
+    def flush_l2(write_only=False):
+        flush.zero_()  # evicts every line of L2 (its own lines stay, dirty)
+        if not write_only:
+            flush_rd.sum()  # evicts those, writing them back; leaves clean lines
 
     def launch(w, dA, dB, dC, bias):
         if nb > 1:
@@ -523,7 +535,7 @@ def run_ours(args, dist):
 
     for _ in range(args.warmup):
         torch.cuda._sleep(HOST_AHEAD_CYCLES)
-        flush.zero_()
+        flush_l2()
         for op in dev_ops:
             launch(*op)
     torch.cuda.synchronize()
@@ -538,7 +550,7 @@ def run_ours(args, dist):
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
         torch.cuda._sleep(HOST_AHEAD_CYCLES)
-        flush.zero_()
+        flush_l2()
         ev = events[s]
         ev[0].record(stream)
         for i, op in enumerate(dev_ops):
@@ -636,25 +648,36 @@ def run_ours(args, dist):
             for _ in range(3):
                 launch(*op)
             torch.cuda.synchronize()
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(reps)]
-            for e0, e1 in evs:
-                if restore:
-                    restore()
-                torch.cuda._sleep(HOST_AHEAD_CYCLES)
-                flush.zero_()
-                e0.record(stream)
-                launch(*op)
-                e1.record(stream)
-            torch.cuda.synchronize()
-            g.binding.check(g.binding.get_device_status(), f"{w.name} device status")
-            times = [e0.elapsed_time(e1) for e0, e1 in evs]
+            def timed_calls(write_only):
+                evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(reps)]
+                for e0, e1 in evs:
+                    if restore:
+                        restore()
+                    torch.cuda._sleep(HOST_AHEAD_CYCLES)
+                    flush_l2(write_only)
+                    e0.record(stream)
+                    launch(*op)
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                g.binding.check(g.binding.get_device_status(), f"{w.name} device status")
+                return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+            times_wo = timed_calls(True)
+            times = timed_calls(False)  # last: its final call's output is checked below
             ms = statistics.mean(times)
+            ms_wo = statistics.mean(times_wo)
             kernels[w.name] = {
                 "ms_mean": ms, "ms_median": statistics.median(times), "ms_min": min(times),
                 "tflops": w.flops / (ms / 1e3) / 1e12, "min_bytes": w.min_bytes(),
                 "achieved_gbs_min_bytes": w.min_bytes() / (ms / 1e3) / 1e9, "calls": reps,
-                "timed": "after the headline timed region, alone, L2 flushed before each call"}
+                "timed": "after the headline timed region, alone, L2 flushed before each call",
+                "write_only_flush": {
+                    "ms_mean": ms_wo, "ms_median": statistics.median(times_wo),
+                    "tflops": w.flops / (ms_wo / 1e3) / 1e12,
+                    "achieved_gbs_min_bytes": w.min_bytes() / (ms_wo / 1e3) / 1e9,
+                    "note": "L2 flushed by the write alone, its dirty lines written back during "
+                            "the call"}}
             rooflines[w.name] = roofline_of(w, ms)
             extra_outputs[w.name] = _host_output(torch, w, dC)  # C restored before the last call
             del dA, dB, dC, dC0
