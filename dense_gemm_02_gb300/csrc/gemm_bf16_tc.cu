@@ -552,6 +552,17 @@ __device__ __forceinline__ void tc_produce_layout(const TcParams &p, const CUten
         tc_producer<BN, true, true, B3>(p, tmA, tmB, ring, full, empty, abort_flag);
 }
 
+// Reads two consecutive 32-column chunks (64 floats) of this thread's
+// accumulator row from tensor memory (columns taddr .. taddr + 63).
+__device__ __forceinline__ void tmem_ld_chunk_pair(uint32_t taddr, float (&x)[2][32]) {
+    uint32_t r0[32], r1[32];
+    tmem_ld_32x32b_x32(taddr, r0);
+    tmem_ld_32x32b_x32(taddr + 32, r1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[0][j] = __uint_as_float(r0[j]), x[1][j] = __uint_as_float(r1[j]);
+}
+
 // Loads two consecutive 32-column chunks (64 floats) of this thread's row
 // of a partial tile from the split-K workspace (float4 i of the pair at
 // src + i * 32: the warp-coalesced workspace layout), all sixteen loads
@@ -813,8 +824,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                                __uint_as_float(r[4 * j + 3])));
                     }
                 }
-                tc_fence_before_sync();
-                mbar_arrive(&tempty[b]);
                 __threadfence();
                 named_bar_sync(TC_EPI_BAR, TC_EPI_THREADS);
                 if (et == 0) {
@@ -822,11 +831,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     *last_flag = (old == (unsigned)(w.nparts - 1)) ? 1 : 0;
                 }
                 named_bar_sync(TC_EPI_BAR, TC_EPI_THREADS);
+                if (!*last_flag) {
+                    tc_fence_before_sync();
+                    mbar_arrive(&tempty[b]);
+                }
                 if (*last_flag && rows_in) {
                     // Last slice of this tile: each thread sums its own row
                     // over slices 0..S-1 in order, two 32-column chunks at a
                     // time with a slice's sixteen loads in flight together,
-                    // then stores the chunks as the plain epilogue does.
+                    // then stores the chunks as the plain epilogue does.  Its
+                    // own slice it reads back from tensor memory (the same
+                    // fp32 values it wrote), so the loads it waits for are
+                    // only the other slices'.
                     __threadfence();
                     const float4 *rq = reinterpret_cast<const float4 *>(p.ws) +
                                        (size_t)tile * p.max_parts * slice4 +
@@ -834,11 +850,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 #pragma unroll 1
                     for (int c = 0; c < BN / 32; c += 2) {
                         float v[2][32];
-                        load_partial_chunks(rq + c * 8 * 32, v);
+                        if (w.part == 0)
+                            tmem_ld_chunk_pair(tbase + c * 32, v);
+                        else
+                            load_partial_chunks(rq + c * 8 * 32, v);
 #pragma unroll 1
                         for (int sl = 1; sl < w.nparts; ++sl) {
                             float x[2][32];
-                            load_partial_chunks(rq + sl * slice4 + c * 8 * 32, x);
+                            if (sl == w.part)
+                                tmem_ld_chunk_pair(tbase + c * 32, x);
+                            else
+                                load_partial_chunks(rq + sl * slice4 + c * 8 * 32, x);
 #pragma unroll
                             for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -858,6 +880,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                 }
                 if (*last_flag) {
+                    tc_fence_before_sync();
+                    mbar_arrive(&tempty[b]);
                     if (et == 0) p.counters[tile] = 0u;  // ready for the next launch
                 }
             }
