@@ -27,6 +27,7 @@ std::atomic<int64_t> g_raster_group{0};
 std::atomic<int64_t> g_cta_pair{0};
 std::atomic<int64_t> g_stream_k{0};
 std::atomic<int64_t> g_pair_limit{0};
+std::atomic<int64_t> g_stage_pairs{0};
 std::atomic<int64_t> g_last_fault{0};
 
 std::mutex g_state_mu;
@@ -35,17 +36,6 @@ DeviceState g_state[kMaxDevices];
 thread_local const char *t_last_kernel = "none";
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;
-
-bool ranges_overlap(const void *a, size_t a_bytes, const void *b, size_t b_bytes) {
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
-}
-
-// Bytes spanned by a rows x cols row-major matrix with pitch ld.
-size_t span_bytes(int64_t rows, int64_t cols, int64_t ld, size_t esz) {
-    if (rows <= 0 || cols <= 0) return 0;
-    return (size_t)((rows - 1) * ld + cols) * esz;
-}
 
 }  // namespace
 
@@ -151,7 +141,7 @@ RuntimeConfig runtime_config() {
     return RuntimeConfig{g_watchdog_ms.load(), g_force_path.load(), g_fault_inject.load(),
                          g_split_k.load(),      g_bf16_tile_n.load(), g_tail_split_off.load(),
                          g_raster_group.load(), g_cta_pair.load(), g_stream_k.load(),
-                         g_pair_limit.load()};
+                         g_pair_limit.load(),   g_stage_pairs.load()};
 }
 
 void consume_fault_inject() { g_fault_inject.store(0); }
@@ -617,6 +607,9 @@ extern "C" int gemm_set_config(const char *key, int64_t value) {
     } else if (!strcmp(key, "pair_limit")) {
         if (value < 0 || value > 1024) return GEMM_ERR_INVALID_ARG;
         g_pair_limit.store(value);
+    } else if (!strcmp(key, "stage_pairs")) {
+        if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
+        g_stage_pairs.store(value);
     } else {
         return GEMM_ERR_INVALID_ARG;
     }
@@ -635,6 +628,7 @@ extern "C" int gemm_get_config(const char *key, int64_t *value) {
     else if (!strcmp(key, "cta_pair")) *value = g_cta_pair.load();
     else if (!strcmp(key, "stream_k")) *value = g_stream_k.load();
     else if (!strcmp(key, "pair_limit")) *value = g_pair_limit.load();
+    else if (!strcmp(key, "stage_pairs")) *value = g_stage_pairs.load();
     else return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }

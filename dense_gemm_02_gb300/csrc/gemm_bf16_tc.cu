@@ -98,6 +98,10 @@ struct TcParams {
     int group_m;     // M-blocks per raster band
     int tiles_main;  // tiles run at full width; the rest are split along N
     int tail_split;  // sub-tiles per tail tile (1, 2 or 4)
+    // CTA-pair kernel: which units run their K blocks two at a time (one
+    // barrier wait and eight MMAs per pair of stages): 0 every unit, 1 the
+    // narrower tail sub-tiles only, 2 none.
+    int stage_pairs;
     float alpha, beta;
     void *C;
     long long ldc;
@@ -466,6 +470,15 @@ __device__ __forceinline__ void load_box_pair(void *dst, const CUtensorMap *map,
         tma_load_2d_pair(dst, map, bar_cl, c0, c1);
 }
 
+// Whether the single-CTA kernel takes its K blocks two at a time (see
+// stage_pairs_for): only with a ring of six or more stages.  Measured on
+// GB300: the packed small-M rings (8 to 12 stages) gain (decode 64 x 8192 x
+// 8192 37.0 -> 36.1 us, a GEMV 36.8 -> 34.8 us), the four-stage ring of the
+// 256-wide tiles loses (4096^3 on this kernel 104 -> 112 us).
+__device__ __forceinline__ bool single_cta_pairs(const TcParams &p) {
+    return p.stage_pairs != 2 && p.stages >= 6;
+}
+
 // TMA producer of the single-CTA kernel (lane 0 of warp 0) for one operand
 // layout: A_MN, A stored K x M (two 64 (M) x 64 (K) boxes per stage); B_KM,
 // B stored N x K (64 (K) x 64 (N) boxes); else row-major A (one 64 (K) x
@@ -479,7 +492,7 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
     using Cfg = TcCfg<BN>;
     const uint32_t S = (uint32_t)p.stages;
     uint32_t it = 0, s = 0, ph = 0;
-    int withheld = -1;
+    int withheld = 0;  // stages the fault-injection hook left unfilled
     bool ok = true;
     Unit w;
     for (int ui = 0; ok && cta_unit<BN>(p, ui, w); ++ui) {
@@ -492,45 +505,69 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
         const uint32_t tx = a_tx + boxes * Cfg::B_BOX_BYTES;
         const int m0 = w.m_blk * TC_BM;
         const int ab = w.bidx * p.a_bmul, bb = w.bidx * p.b_bmul;  // batch coordinates
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
+        // Copies of K block kb into stage st, completing on `bar`.
+        auto load_stage = [&](uint32_t st, int kb, uint64_t *bar) {
+            uint8_t *a_dst = ring + st * (uint32_t)p.stage_bytes;
+            uint8_t *b_dst = a_dst + p.a_slot;
+            const int k0 = kb * TC_BK;
+            if constexpr (A_MN) {
+                load_box<B3>(a_dst, tmA, bar, m0, k0, ab);
+                if (p.a_rows > 64) load_box<B3>(a_dst + 8192, tmA, bar, m0 + 64, k0, ab);
+            } else {
+                load_box<B3>(a_dst, tmA, bar, k0, m0, ab);
+            }
+            for (int j = 0; j < boxes; ++j) {
+                if constexpr (B_KM)
+                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, bar, k0, w.n0 + j * 64, bb);
+                else
+                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, bar, w.n0 + j * 64, k0, bb);
+            }
+        };
+        const bool paired = single_cta_pairs(p);
+        for (int kb = w.kb0; kb < w.kb1 && ok;) {
+            // Paired (as in the CTA-pair kernel): K blocks kb and kb + 1 go to
+            // consecutive stages cur and nxt, both completing on full[cur];
+            // full[nxt] is arrived at once to keep its phase in step.
+            const bool two = paired && kb + 1 < w.kb1;
             const uint32_t cur = s, cur_ph = ph;
             if (++s == S) {
                 s = 0;
                 ph ^= 1u;
             }
-            if (!mbar_wait(&empty[cur], cur_ph ^ 1u, abort_flag, p.timeout_ns)) {
+            uint32_t nxt = 0, nxt_ph = 0;
+            if (two) {
+                nxt = s;
+                nxt_ph = ph;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!mbar_wait(&empty[cur], cur_ph ^ 1u, abort_flag, p.timeout_ns) ||
+                (two && !mbar_wait(&empty[nxt], nxt_ph ^ 1u, abort_flag, p.timeout_ns))) {
                 record_fault(p, abort_flag, kRoleProducer, cur, w.tile);
                 ok = false;
                 break;
             }
+            const int step = two ? 2 : 1;
             if (p.fault_inject && blockIdx.x == 0 && it == 0) {
-                withheld = 0;  // test hook: this stage is never filled
+                withheld = step;  // test hook: these stages are never filled
+                it += step;
+                kb += step;
                 continue;
             }
-            mbar_arrive_expect_tx(&full[cur], tx);
-            uint8_t *a_dst = ring + cur * (uint32_t)p.stage_bytes;
-            uint8_t *b_dst = a_dst + p.a_slot;
-            const int k0 = kb * TC_BK;
-            if constexpr (A_MN) {
-                load_box<B3>(a_dst, tmA, &full[cur], m0, k0, ab);
-                if (p.a_rows > 64) load_box<B3>(a_dst + 8192, tmA, &full[cur], m0 + 64, k0, ab);
-            } else {
-                load_box<B3>(a_dst, tmA, &full[cur], k0, m0, ab);
-            }
-            for (int j = 0; j < boxes; ++j) {
-                if constexpr (B_KM)
-                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[cur], k0,
-                                 w.n0 + j * 64, bb);
-                else
-                    load_box<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, &full[cur], w.n0 + j * 64,
-                                 k0, bb);
-            }
+            mbar_arrive_expect_tx(&full[cur], (uint32_t)step * tx);
+            if (two) mbar_arrive(&full[nxt]);
+            load_stage(cur, kb, &full[cur]);
+            if (two) load_stage(nxt, kb + 1, &full[cur]);
+            it += step;
+            kb += step;
         }
     }
     // Let every copy started here land before the CTA can exit.
     const uint32_t first = it > S ? it - S : 0u;
     for (uint32_t i = first; i < it; ++i) {
-        if ((int)i == withheld) continue;
+        if ((int)i < withheld) continue;  // withheld: the first 1 or 2 stages
         mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
     }
 }
@@ -721,7 +758,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
                 uint32_t acc = 0;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                const bool paired = single_cta_pairs(p);
+                for (int kb = w.kb0; kb < w.kb1;) {
+                    // Paired: stages s and s + 1 both completed on full[s].
+                    const bool two = paired && kb + 1 < w.kb1;
                     const bool ready = mbar_wait(&full[s], ph, abort_flag, p.timeout_ns);
                     if (__any_sync(0xffffffffu, !ready)) {
                         if (lane == 0) record_fault(p, abort_flag, kRoleMma, s, w.tile);
@@ -741,6 +781,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         s = 0;
                         ph ^= 1u;
                     }
+                    if (two) {
+                        const uint64_t ad2 = desc_add(a_desc0, s * stage_bytes);
+                        const uint64_t bd2 = desc_add(b_desc0, s * stage_bytes);
+                        umma_f16_elect(d_tmem, ad2, bd2, idesc, 1u);
+                        umma_f16_elect(d_tmem, ad2 + a1, bd2 + b1, idesc, 1u);
+                        umma_f16_elect(d_tmem, ad2 + a2, bd2 + b2, idesc, 1u);
+                        umma_f16_elect(d_tmem, ad2 + a3, bd2 + b3, idesc, 1u);
+                        umma_commit_elect(&empty[s]);
+                        if (++s == S) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    kb += two ? 2 : 1;
                 }
                 if (!ok) break;
                 umma_commit_elect(&tfull[b]);  // accumulator b is complete
@@ -932,6 +986,20 @@ struct Tc2Cfg {
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 };
 
+// Whether a unit of the CTA-pair kernel runs its K blocks two at a time:
+// one barrier wait (with its warp vote and fence) per two 64-deep stages,
+// then eight MMAs.  Measured on GB300 (per-stage clock stamps of the issuing
+// warp): the wait costs about 67 ns even when the data is there and four
+// MMA issues and a commit about 150-175 ns, so a 64-deep stage costs the
+// issuer about 255-280 ns, as long as the four M = 256, N = 256 MMAs
+// execute (262 ns) and twice as long as four N = 128 ones (131 ns, the
+// tail's column halves).  Paired stages leave the tensor pipe the slack:
+// 4096^3 90.2 -> 86.8 us pairing only the column halves, 80.1 us pairing
+// every tile; the MLP shape 516 -> 470 us; 8192^3 576 -> 549 us.
+__device__ __forceinline__ bool stage_pairs_for(const TcParams &p, const Unit &w) {
+    return p.stage_pairs == 0 || (p.stage_pairs == 1 && w.width < Tc2Cfg::BN);
+}
+
 // TMA producer of the CTA-pair kernel (lane 0 of warp 0 in both CTAs), for
 // one operand layout (as tc_producer).  Each CTA loads its own 128 rows of A
 // and its half of the tile's B columns; all copies complete on the even
@@ -946,7 +1014,7 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
     constexpr int S = Cfg::STAGES;
     const bool leader = (rank == 0);
     uint32_t it = 0;
-    int withheld = -1;
+    int withheld = 0;  // stages the fault-injection hook left unfilled
     bool ok = true;
     for (int u = pair; u < p.num_units && ok; u += npairs) {
         const Unit w = decode_unit<Cfg::BN>(p, u);
@@ -957,21 +1025,10 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
         const int row0 = w.m_blk * 2 * TC_BM + (int)rank * TC_BM;
         const int col0 = w.n0 + (int)rank * half;
         const int ab = w.bidx * p.a_bmul, bb = w.bidx * p.b_bmul;  // batch coordinates
-        for (int kb = w.kb0; kb < w.kb1; ++kb, ++it) {
-            const int s = it % S;
-            const uint32_t ph = (it / S) & 1u;
-            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) {
-                record_fault(p, abort_flag, kRoleProducer, s, w.tile);
-                ok = false;
-                break;
-            }
-            if (p.fault_inject && pair == 0 && leader && it == 0) {
-                withheld = 0;  // test hook: the stage's barrier never completes
-                continue;
-            }
-            const uint32_t full_cl = mapa_shared(smem_addr(&full[s]), 0);
-            if (leader) mbar_arrive_expect_tx(&full[s], tx);
-            uint8_t *a_dst = sA + s * Cfg::A_BYTES;
+        // Copies of K block kb into stage st, completing on the even CTA's
+        // barrier full_cl.
+        auto load_stage = [&](int st, int kb, uint32_t full_cl) {
+            uint8_t *a_dst = sA + st * Cfg::A_BYTES;
             const int k0 = kb * TC_BK;
             if constexpr (A_MN) {
                 load_box_pair<B3>(a_dst, tmA, full_cl, row0, k0, ab);
@@ -979,7 +1036,7 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
             } else {
                 load_box_pair<B3>(a_dst, tmA, full_cl, k0, row0, ab);
             }
-            uint8_t *b_dst = sB + s * Cfg::B_BYTES;
+            uint8_t *b_dst = sB + st * Cfg::B_BYTES;
             for (int j = 0; j < boxes; ++j) {
                 if constexpr (B_KM)
                     load_box_pair<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, full_cl, k0,
@@ -988,6 +1045,39 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
                     load_box_pair<B3>(b_dst + j * Cfg::B_BOX_BYTES, tmB, full_cl,
                                       col0 + j * 64, k0, bb);
             }
+        };
+        const bool paired = stage_pairs_for(p, w);
+        for (int kb = w.kb0; kb < w.kb1 && ok;) {
+            // Paired: K blocks kb and kb + 1 go to consecutive stages s and s2
+            // and both complete on full[s]; full[s2] is arrived at once (no
+            // bytes), which keeps its phase in step with the ring.
+            const bool two = paired && kb + 1 < w.kb1;
+            const int s = it % S;
+            const uint32_t ph = (it / S) & 1u;
+            const int s2 = (it + 1) % S;
+            const uint32_t ph2 = ((it + 1) / S) & 1u;
+            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns) ||
+                (two && !mbar_wait(&empty[s2], ph2 ^ 1u, abort_flag, p.timeout_ns))) {
+                record_fault(p, abort_flag, kRoleProducer, s, w.tile);
+                ok = false;
+                break;
+            }
+            const int step = two ? 2 : 1;
+            if (p.fault_inject && pair == 0 && leader && it == 0) {
+                withheld = two ? 2 : 1;  // test hook: the stage's barrier never completes
+                it += step;
+                kb += step;
+                continue;
+            }
+            const uint32_t full_cl = mapa_shared(smem_addr(&full[s]), 0);
+            if (leader) {
+                mbar_arrive_expect_tx(&full[s], (uint32_t)step * tx);
+                if (two) mbar_arrive(&full[s2]);
+            }
+            load_stage(s, kb, full_cl);
+            if (two) load_stage(s2, kb + 1, full_cl);
+            it += step;
+            kb += step;
         }
     }
     // The even CTA's full barriers count both CTAs' copies: wait for the
@@ -995,7 +1085,7 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
     if (leader) {
         const uint32_t first = it > (uint32_t)S ? it - S : 0u;
         for (uint32_t i = first; i < it; ++i) {
-            if ((int)i == withheld) continue;
+            if ((int)i < withheld) continue;  // withheld: the first 1 or 2 stages
             mbar_wait(&full[i % S], (i / S) & 1u, abort_flag, p.timeout_ns, true);
         }
     }
@@ -1114,7 +1204,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
                 uint32_t acc = 0;
-                for (int kb = w.kb0; kb < w.kb1; ++kb) {
+                const bool paired = stage_pairs_for(p, w);
+                for (int kb = w.kb0; kb < w.kb1;) {
+                    // Paired: stages s and s + 1 both completed on full[s].
+                    const bool two = paired && kb + 1 < w.kb1;
                     const bool ready = mbar_wait(&full[s], ph, abort_flag, p.timeout_ns);
                     if (__any_sync(0xffffffffu, !ready)) {
                         if (lane == 0) record_fault(p, abort_flag, kRoleMma, s, w.tile);
@@ -1134,6 +1227,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                         s = 0;
                         ph ^= 1u;
                     }
+                    if (two) {
+                        const uint64_t ad2 = desc_add(a_desc0, s * Cfg::A_BYTES);
+                        const uint64_t bd2 = desc_add(b_desc0, s * Cfg::B_BYTES);
+                        umma_f16_pair_elect(d_tmem, ad2, bd2, idesc, 1u);
+                        umma_f16_pair_elect(d_tmem, ad2 + a1, bd2 + b1, idesc, 1u);
+                        umma_f16_pair_elect(d_tmem, ad2 + a2, bd2 + b2, idesc, 1u);
+                        umma_f16_pair_elect(d_tmem, ad2 + a3, bd2 + b3, idesc, 1u);
+                        umma_commit_pair_elect(&empty[s], 0x3);
+                        if (++s == (uint32_t)S) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    kb += two ? 2 : 1;
                 }
                 if (!ok) break;
                 umma_commit_pair_elect(&tfull[b], 0x3);  // accumulator b complete in both CTAs
@@ -1629,6 +1736,7 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
     p.tiles_per_batch = (int)tiles_per_batch;
     int splits = 1;
     const RuntimeConfig cfg = runtime_config();
+    p.stage_pairs = (int)cfg.stage_pairs;
     // Few tiles (at most half the SMs) and a long K: split K.  By default
     // into equal slices per tile (as many as keep the SMs busy); with
     // `stream_k` set, stream-K instead: all tiles * num_kb K iterations are
@@ -1800,6 +1908,7 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
         }) != 0)
         return GEMM_ERR_CUDA;
     const RuntimeConfig cfg = runtime_config();
+    p.stage_pairs = (int)cfg.stage_pairs;
     int pairs_max = max_resident_pairs(device);
     if (pairs_max <= 0) return GEMM_ERR_CUDA;
     if (cfg.pair_limit > 0 && cfg.pair_limit < pairs_max) pairs_max = (int)cfg.pair_limit;

@@ -103,6 +103,7 @@ struct RuntimeConfig {
     int64_t cta_pair;
     int64_t stream_k;
     int64_t pair_limit;
+    int64_t stage_pairs;
 };
 RuntimeConfig runtime_config();
 void consume_fault_inject();
@@ -183,6 +184,18 @@ cudaError_t launch_gemm_simt_generic(int M, int N, int K, float alpha, const voi
 // matrices stride_c elements apart.
 cudaError_t launch_scale_c(int M, int N, float beta, void *C, int64_t ldc, bool c_f32,
                            int64_t batch, int64_t stride_c, cudaStream_t stream);
+
+// Whether the byte ranges [a, a + a_bytes) and [b, b + b_bytes) meet.
+inline bool ranges_overlap(const void *a, size_t a_bytes, const void *b, size_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+// Bytes spanned by a rows x cols row-major matrix with pitch ld.
+inline size_t span_bytes(int64_t rows, int64_t cols, int64_t ld, size_t esz) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return (size_t)((rows - 1) * ld + cols) * esz;
+}
 
 // Host-side argument checks shared by the entry points.  Returns GEMM_OK,
 // an error, or 1 for "valid, nothing to do" (M == 0 or N == 0).

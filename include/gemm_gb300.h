@@ -268,6 +268,34 @@ GEMM_API int gemm_bf16_host(int64_t M, int64_t N, int64_t K, float alpha, const 
                             int64_t ldc, int c_type);
 
 /*
+ * Several host-buffer GEMMs in one call.  The products run in order through
+ * the pipeline above: the copies of product i + 1 are enqueued right behind
+ * those of product i, so they travel while product i computes, and the call
+ * returns once every C holds its result.  (A sequence of gemm_*_host calls
+ * cannot overlap this way: each returns only when its C is back.)  Each
+ * product follows the rules of gemm_f32_host / gemm_bf16_host; in addition
+ * no product's C may overlap an operand or the C of another product of the
+ * batch (GEMM_ERR_ALIAS): products that feed one another need separate calls.
+ * At most GEMM_HOST_BATCH_MAX products; count == 0 does nothing.  The pages
+ * have no counterpart (their GEMMs start from device memory).
+ */
+enum { GEMM_HOST_F32 = 0, GEMM_HOST_BF16 = 1 };
+#define GEMM_HOST_BATCH_MAX 64
+typedef struct {
+    int dtype;    /* GEMM_HOST_F32: fp32 A, B, C; GEMM_HOST_BF16: bf16 A, B */
+    int c_type;   /* GEMM_HOST_BF16 only: GEMM_OUT_BF16 or GEMM_OUT_F32 */
+    int64_t M, N, K;
+    float alpha, beta;
+    const void *A;
+    int64_t lda;  /* elements, row-major M x K */
+    const void *B;
+    int64_t ldb;  /* elements, row-major K x N */
+    void *C;
+    int64_t ldc;  /* elements, row-major M x N */
+} gemm_host_op_t;
+GEMM_API int gemm_host_batch(int64_t count, const gemm_host_op_t *ops);
+
+/*
  * Allocation-free BF16 GEMM.  The source pages have no counterpart: this is
  * an interface for callers that cannot call cudaMalloc at all, for example
  * code that runs inside a host whose device memory is fully owned by its own
@@ -363,6 +391,11 @@ GEMM_API const char *gemm_status_string(int status);
  *   "pair_limit"    0 all resident pairs, else at most this many CTA pairs
  *                   (leaves SMs free for other work; tests use it to reach
  *                   the tail paths at small sizes)
+ *   "stage_pairs"   tcgen05 kernels: 0 (default) every tile runs its K
+ *                   blocks two at a time (one barrier wait and eight MMAs per
+ *                   pair of stages; the single-CTA kernel only when its ring
+ *                   has six or more stages), 1 on the CTA-pair kernel only its
+ *                   narrower tail tiles, 2 none
  * Returns GEMM_OK or GEMM_ERR_INVALID_ARG for an unknown key or value.
  */
 GEMM_API int gemm_set_config(const char *key, int64_t value);

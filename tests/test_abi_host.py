@@ -163,7 +163,7 @@ def test_config_keys(lib):
     # every documented key round-trips its default and rejects a bad value
     for key, bad in (("force_path", 3), ("fault_inject", 2), ("split_k", 65), ("bf16_tile_n", 64),
                      ("tail_split_off", 2), ("stream_k", 2), ("raster_group", -1),
-                     ("cta_pair", 3), ("pair_limit", -1)):
+                     ("cta_pair", 3), ("pair_limit", -1), ("stage_pairs", 3)):
         v = b.get_config(key)
         b.set_config(key, v)
         with pytest.raises(b.GemmError):
@@ -230,3 +230,45 @@ def test_grouped_entry_point_errors(lib):
         assert grouped(b.make_groups([ok[0], prob(C0, B1, C1)]), 2) == b.GEMM_ERR_ALIAS
         # (shared read-only operands are allowed: tested on the GPU with
         # real buffers, since a call that passes the checks launches)
+
+
+def test_host_batch_entry_point_errors(lib):
+    """gemm_host_batch: the count, every product's checks and the
+    cross-product overlap check run before any CUDA call."""
+    from dense_gemm_02_gb300 import binding as b
+
+    fake = 1 << 24
+    F32, BF = b.GEMM_HOST_F32, b.GEMM_HOST_BF16
+
+    def op(A, B, C, dtype=F32, c_type=b.GEMM_OUT_F32, M=4, N=4, K=4, lda=4, ldb=4, ldc=4,
+           alpha=1.0, beta=0.0):
+        return (dtype, c_type, M, N, K, alpha, beta, A, lda, B, ldb, C, ldc)
+
+    A0, B0, C0 = fake, fake + 4096, fake + 8192
+    A1, B1, C1 = fake + 12288, fake + 16384, fake + 20480
+    ok = [op(A0, B0, C0), op(A1, B1, C1, dtype=BF)]
+    assert b.gemm_host_batch(b.make_host_ops([]), -1) == b.GEMM_ERR_INVALID_ARG
+    assert b.gemm_host_batch(b.make_host_ops(ok), b.GEMM_HOST_BATCH_MAX + 1) == \
+        b.GEMM_ERR_INVALID_ARG
+    assert b.gemm_host_batch(None, 0) == b.GEMM_OK  # nothing to do
+    assert b.gemm_host_batch(None, 2) == b.GEMM_ERR_NULLPTR
+    # products with M == 0 or N == 0 are skipped: a batch of them does nothing
+    assert b.gemm_host_batch(b.make_host_ops([op(A0, B0, C0, M=0), op(A1, B1, C1, N=0)]), 2) == \
+        b.GEMM_OK
+    # an unknown element type, a bad output type for a bf16 product
+    assert b.gemm_host_batch(b.make_host_ops([ok[0], op(A1, B1, C1, dtype=7)]), 2) == \
+        b.GEMM_ERR_INVALID_ARG
+    assert b.gemm_host_batch(b.make_host_ops([ok[0], op(A1, B1, C1, dtype=BF, c_type=5)]), 2) == \
+        b.GEMM_ERR_INVALID_ARG
+    # a bad pitch or a missing operand in the second product
+    assert b.gemm_host_batch(b.make_host_ops([ok[0], op(A1, B1, C1, ldb=2)]), 2) == \
+        b.GEMM_ERR_BAD_LD
+    assert b.gemm_host_batch(b.make_host_ops([ok[0], op(A1, None, C1)]), 2) == \
+        b.GEMM_ERR_NULLPTR
+    # C overlapping its own A (the single-product rule)
+    assert b.gemm_host_batch(b.make_host_ops([op(A0, B0, A0 + 4)]), 1) == b.GEMM_ERR_ALIAS
+    # product 1 writes into product 0's A, B or C, or reads product 0's C
+    for target in (A0, B0, C0 + 8):
+        assert b.gemm_host_batch(b.make_host_ops([ok[0], op(A1, B1, target)]), 2) == \
+            b.GEMM_ERR_ALIAS, target
+    assert b.gemm_host_batch(b.make_host_ops([ok[0], op(C0, B1, C1)]), 2) == b.GEMM_ERR_ALIAS

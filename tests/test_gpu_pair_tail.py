@@ -1,9 +1,11 @@
 """GPU parity of the CTA-pair kernel's partial last wave at sizes the oracle
 finishes in seconds.  When the tile count leaves a partial wave, each of its
 tiles is cut into two 128-column halves so that twice as many pairs share
-it (a half wholly past the N edge is skipped).  The "pair_limit" knob caps
-the pair count so that small problems reach this path, as 4096^3 does on
-76 pairs (256 tiles: 28 in the partial wave).
+it (a half wholly past the N edge is skipped); the halves run their K
+blocks two at a time (one barrier wait and eight MMAs per pair of stages),
+as every tile does ("stage_pairs" 0; 1: only the halves, 2: none).  The
+"pair_limit" knob caps the pair count so that small problems reach this
+path, as 4096^3 does on 76 pairs (256 tiles: 28 in the partial wave).
 
 Integer-valued operands make every sum exact, so results must match the
 oracle bit for bit with and without the split ("tail_split_off"); random
@@ -85,15 +87,18 @@ def ref_round(R, out):
     return oracle.round_bf16(R) if out == "bf16" else oracle.round_f32(R)
 
 
+# "stage_pairs": 0 every tile runs its K blocks two at a time, 1 only the
+# column halves do, 2 none
+@pytest.mark.parametrize("stage_pairs", [0, 1, 2])
 @pytest.mark.parametrize("tail_off", [0, 1])
 @pytest.mark.parametrize("out", ["bf16", "f32"])
 @pytest.mark.parametrize("P,M,N,K", CASES)
-def test_partial_wave_integer_bit_exact(P, M, N, K, out, tail_off):
+def test_partial_wave_integer_bit_exact(P, M, N, K, out, tail_off, stage_pairs):
     seed = 16000 + P + M + N + K + (out == "f32")
     A = gi.draw("integer", seed, 0, (M, K), dtype="bf16")
     B = gi.draw("integer", seed, 1, (K, N), dtype="bf16")
     Cin = gi.draw("integer", seed, 2, (M, N), dtype=out)
-    with config(cta_pair=2, pair_limit=P, tail_split_off=tail_off):
+    with config(cta_pair=2, pair_limit=P, tail_split_off=tail_off, stage_pairs=stage_pairs):
         C = run(A, B, Cin, 0.5, -1.0, out)
     assert B_.last_kernel() == "bf16_tcgen05"
     got, ref = C.result(), ref_round(oracle.gemm(A, B, Cin, alpha=0.5, beta=-1.0), out)
@@ -116,12 +121,13 @@ def test_partial_wave_layouts_bias_relu_integer(ta, tb):
 
 
 @pytest.mark.parametrize("out", ["bf16", "f32"])
-def test_partial_wave_normal_tolerance_and_repeatable(out):
+@pytest.mark.parametrize("stage_pairs", [0, 1])
+def test_partial_wave_normal_tolerance_and_repeatable(out, stage_pairs):
     P, M, N, K = 7, 1280, 512, 2056
     assert tail_info(M, N, K, P)[1]
     A = gi.draw("normal", 16300, 0, (M, K), dtype="bf16")
     B = gi.draw("normal", 16300, 1, (K, N), dtype="bf16")
-    with config(cta_pair=2, pair_limit=P):
+    with config(cta_pair=2, pair_limit=P, stage_pairs=stage_pairs):
         C1 = run(A, B, None, 1.0, 0.0, out)
         C2 = run(A, B, None, 1.0, 0.0, out)
     assert np.array_equal(C1.result(), C2.result())
@@ -162,14 +168,15 @@ def test_partial_wave_through_the_allocation_free_entry():
     assert np.array_equal(C.cpu().numpy(), oracle.round_f32(oracle.gemm(A, B)))
 
 
-def test_pair_kernel_watchdog_and_recovery():
+@pytest.mark.parametrize("stage_pairs", [0, 1])
+def test_pair_kernel_watchdog_and_recovery(stage_pairs):
     P, M, N, K = CASES[0]
     seed = 16600
     A = gi.draw("integer", seed, 0, (M, K), dtype="bf16")
     B = gi.draw("integer", seed, 1, (K, N), dtype="bf16")
     dA, dB = bf16_to_dev(A), bf16_to_dev(B)
     C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
-    with config(cta_pair=2, pair_limit=P, watchdog_ms=200):
+    with config(cta_pair=2, pair_limit=P, watchdog_ms=200, stage_pairs=stage_pairs):
         g.set_config("fault_inject", 1)
         try:
             g.gemm_bf16(dA, dB, C, out_dtype=torch.float32)

@@ -234,9 +234,13 @@ def test_bf16_pitched_operands(pads):
     assert C.guards_intact()
 
 
+# stage_pairs 0 (default): K blocks two at a time where the ring is deep
+# enough (the 128-wide tiles' six stages, the slices' odd block counts
+# ending on a single stage); 2: one at a time
+@pytest.mark.parametrize("stage_pairs", [0, 2])
 @pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("split_k", [1, 2, 3, 5])
-def test_bf16_tiles_and_split_k_integer(tile_n, split_k):
+def test_bf16_tiles_and_split_k_integer(tile_n, split_k, stage_pairs):
     M, N, K = 192, 640, 1536
     seed = 99 + tile_n + split_k
     A = gi.draw("integer", seed, 0, (M, K), dtype="bf16")
@@ -244,11 +248,13 @@ def test_bf16_tiles_and_split_k_integer(tile_n, split_k):
     Cin = gi.draw("integer", seed, 2, (M, N), dtype="f32")
     g.set_config("bf16_tile_n", tile_n)
     g.set_config("split_k", split_k)
+    g.set_config("stage_pairs", stage_pairs)
     try:
         C = run_bf16(A, B, Cin, 1.0, 1.0, "f32")
     finally:
         g.set_config("bf16_tile_n", 0)
         g.set_config("split_k", 0)
+        g.set_config("stage_pairs", 0)
     ref = oracle.round_f32(oracle.gemm(A, B, Cin, alpha=1.0, beta=1.0))
     assert np.array_equal(C.result(), ref)
     assert C.guards_intact()
