@@ -7,10 +7,11 @@ bias / activation epilogue.  This package is the thin Python binding.
 """
 
 from . import binding
-from .api import gemm, gemm_batched, gemm_bf16, gemm_ex, gemm_grouped, sgemm
+from .api import gemm, gemm_batched, gemm_bf16, gemm_ex, gemm_grouped, gemm_many, sgemm
 from .binding import GemmError, get_config, set_config
 
-__all__ = ["gemm", "gemm_batched", "gemm_bf16", "gemm_ex", "gemm_grouped", "sgemm", "binding",
+__all__ = ["gemm", "gemm_batched", "gemm_bf16", "gemm_ex", "gemm_grouped", "gemm_many", "sgemm",
+           "binding",
            "GemmError", "get_config", "set_config", "flops"]
 
 

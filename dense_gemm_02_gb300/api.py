@@ -314,9 +314,26 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
     """
     if A.is_cuda:
         return _dispatch(A, B, C, alpha, beta, out_dtype, stream)
+    op, out, _keep = _host_op(A, B, C, alpha, beta, out_dtype, out)
+    with torch.cuda.device(device):
+        if op[0] == _b.GEMM_HOST_F32:
+            rc = _b.gemm_f32_host(*op[2:5], op[5], op[7], op[8], op[9], op[10], op[6], op[11],
+                                  op[12])
+            _b.check(rc, "gemm_f32_host")
+        else:
+            rc = _b.gemm_bf16_host(*op[2:5], op[5], op[7], op[8], op[9], op[10], op[6], op[11],
+                                   op[12], op[1])
+            _b.check(rc, "gemm_bf16_host")
+    return out
+
+
+def _host_op(A, B, C, alpha, beta, out_dtype, out):
+    """Checks one host-buffer product and returns (gemm_host_op_t fields,
+    out, tensors to keep alive): out is the given one, C, or a new pinned
+    tensor, already holding C when beta != 0."""
     if A.dtype != B.dtype or A.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("A and B must both be float32 or both bfloat16")
-    if B.is_cuda or (C is not None and C.is_cuda) or (out is not None and out.is_cuda):
+    if A.is_cuda or B.is_cuda or (C is not None and C.is_cuda) or (out is not None and out.is_cuda):
         raise TypeError("host-buffer call: A, B, C and out must all be host tensors")
     M, N, K = _shapes(A, B, C)
     if A.dtype == torch.float32:
@@ -333,20 +350,33 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None,
         out.copy_(C)  # the library updates C in place
     A = A if (A.dim() == 2 and (A.size(1) <= 1 or A.stride(1) == 1)) else A.contiguous()
     B = B if (B.dim() == 2 and (B.size(1) <= 1 or B.stride(1) == 1)) else B.contiguous()
-    ldo = _row_major(out, "out")
+    f32 = A.dtype == torch.float32
+    op = (_b.GEMM_HOST_F32 if f32 else _b.GEMM_HOST_BF16,
+          _b.GEMM_OUT_F32 if od == torch.float32 else _b.GEMM_OUT_BF16,
+          M, N, K, float(alpha), float(beta), A.data_ptr(), _row_major(A, "A"),
+          B.data_ptr(), _row_major(B, "B"), out.data_ptr(), _row_major(out, "out"))
+    return op, out, (A, B)
+
+
+def gemm_many(problems, device="cuda") -> list:
+    """Several host-buffer products C_i = alpha_i * A_i @ B_i + beta_i * C_i
+    in one library call (gemm_host_batch): the copies of product i + 1 travel
+    while product i computes, and the call returns once every result is in
+    host memory.  ``problems`` is a sequence of dicts with the keys of
+    :func:`gemm` (A, B and optionally C, alpha, beta, out_dtype, out), all
+    host tensors.  No result may share memory with another product's
+    operands or result.  Returns the outputs in order."""
+    ops, outs, keep = [], [], []
+    for pr in problems:
+        op, out, k = _host_op(pr["A"], pr["B"], pr.get("C"), pr.get("alpha", 1.0),
+                              pr.get("beta", 0.0), pr.get("out_dtype"), pr.get("out"))
+        ops.append(op)
+        outs.append(out)
+        keep.append(k)
+    arr = _b.make_host_ops(ops)
     with torch.cuda.device(device):
-        if A.dtype == torch.float32:
-            rc = _b.gemm_f32_host(M, N, K, float(alpha), A.data_ptr(), _row_major(A, "A"),
-                                  B.data_ptr(), _row_major(B, "B"), float(beta), out.data_ptr(),
-                                  ldo)
-            _b.check(rc, "gemm_f32_host")
-        else:
-            c_type = _b.GEMM_OUT_F32 if od == torch.float32 else _b.GEMM_OUT_BF16
-            rc = _b.gemm_bf16_host(M, N, K, float(alpha), A.data_ptr(), _row_major(A, "A"),
-                                   B.data_ptr(), _row_major(B, "B"), float(beta), out.data_ptr(),
-                                   ldo, c_type)
-            _b.check(rc, "gemm_bf16_host")
-    return out
+        _b.check(_b.gemm_host_batch(arr, len(ops)), "gemm_host_batch")
+    return outs
 
 
 def _dispatch(A, B, C, alpha, beta, out_dtype, stream):

@@ -32,6 +32,10 @@ GEMM_ACT_NONE = 0
 GEMM_ACT_RELU = 1
 GEMM_ACT_GELU_TANH = 2
 
+GEMM_HOST_F32 = 0
+GEMM_HOST_BF16 = 1
+GEMM_HOST_BATCH_MAX = 64
+
 
 class GemmOpts(ctypes.Structure):
     """gemm_opts_t: operand layouts and fused epilogue of the *_ex calls."""
@@ -50,6 +54,16 @@ class GemmGroup(ctypes.Structure):
                 ("alpha", ctypes.c_float), ("beta", ctypes.c_float)]
 
 # Every exported symbol of the C ABI, with (restype, argtypes).
+class GemmHostOp(ctypes.Structure):
+    """gemm_host_op_t: one product of gemm_host_batch (host addresses)."""
+
+    _fields_ = [("dtype", ctypes.c_int), ("c_type", ctypes.c_int), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("alpha", ctypes.c_float),
+                ("beta", ctypes.c_float), ("A", ctypes.c_void_p), ("lda", ctypes.c_int64),
+                ("B", ctypes.c_void_p), ("ldb", ctypes.c_int64), ("C", ctypes.c_void_p),
+                ("ldc", ctypes.c_int64)]
+
+
 _i64, _f32, _vp, _int, _cp = (ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_int,
                               ctypes.c_char_p)
 SIGNATURES = {
@@ -70,6 +84,7 @@ SIGNATURES = {
                                  _vp]),
     "gemm_f32_grouped": (_int, [_i64, ctypes.POINTER(GemmGroup), ctypes.POINTER(GemmOpts), _vp]),
     "gemm_f32_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64]),
+    "gemm_host_batch": (_int, [_i64, ctypes.POINTER(GemmHostOp)]),
     "gemm_bf16_host": (_int, [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64,
                               _int]),
     "gemm_noalloc_get_status": (_int, [_vp, ctypes.POINTER(_i64)]),
@@ -209,6 +224,20 @@ def gemm_f32_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:
 def gemm_bf16_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type) -> int:
     """Raw call of the host-buffer BF16 GEMM; A, B, C are host addresses."""
     return lib().gemm_bf16_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, c_type)
+
+
+def make_host_ops(problems) -> ctypes.Array:
+    """A gemm_host_op_t array from (dtype, c_type, M, N, K, alpha, beta, A,
+    lda, B, ldb, C, ldc) tuples (A, B, C host addresses)."""
+    arr = (GemmHostOp * max(1, len(problems)))()
+    for i, pr in enumerate(problems):
+        arr[i] = GemmHostOp(*pr)
+    return arr
+
+
+def gemm_host_batch(ops, count) -> int:
+    """Raw call of the batched host-buffer GEMM; ops from make_host_ops."""
+    return lib().gemm_host_batch(count, ops)
 
 
 def noalloc_get_status(stream=None) -> tuple[int, int]:

@@ -120,3 +120,55 @@ def test_host_entry_rejects_overlap_and_bad_type():
     rc = b.gemm_bf16_host(64, 64, 64, 1.0, Ab.data_ptr(), 64, Ab.data_ptr(), 64, 0.0,
                           Cb.data_ptr(), 64, 7)
     assert rc == b.GEMM_ERR_INVALID_ARG
+
+
+def test_host_batch_mixed_products_integer_bit_exact():
+    """gemm_many / gemm_host_batch: an FP32 product with several row blocks,
+    a BF16 product into bf16 with beta != 0 and pitched operands, and a BF16
+    product into fp32, in one pipelined call; each bit for bit against the
+    oracle and equal to its single call."""
+    seed = 14400
+    Af = gi.draw("integer", seed, 0, (2100, 520))
+    Bf = gi.draw("integer", seed, 1, (520, 264))
+    Ab = gi.draw("integer", seed + 1, 0, (600, 136), dtype="bf16")
+    Bb = gi.draw("integer", seed + 1, 1, (136, 1000), dtype="bf16")
+    Cb = gi.draw("integer", seed + 1, 2, (600, 1000), dtype="bf16")
+    Ac = gi.draw("integer", seed + 2, 0, (33, 4096), dtype="bf16")
+    Bc = gi.draw("integer", seed + 2, 1, (4096, 72), dtype="bf16")
+    hCb = host(Cb, "bf16")
+    outs = g.gemm_many([
+        dict(A=host(Af, "f32"), B=host(Bf, "f32", pad=2), alpha=2.0),
+        dict(A=host(Ab, "bf16", pad=3), B=host(Bb, "bf16", pad=5), C=hCb, alpha=0.5, beta=-1.0),
+        dict(A=host(Ac, "bf16"), B=host(Bc, "bf16"), out_dtype=torch.float32),
+    ])
+    assert outs[1].data_ptr() == hCb.data_ptr()  # C updated in place
+    refs = [oracle.round_f32(oracle.gemm(Af, Bf, alpha=2.0)),
+            oracle.round_bf16(oracle.gemm(Ab, Bb, Cb, alpha=0.5, beta=-1.0)),
+            oracle.round_f32(oracle.gemm(Ac, Bc))]
+    for i, (o, r) in enumerate(zip(outs, refs)):
+        got = result(o)
+        assert np.array_equal(got, r), f"product {i}: {int((got != r).sum())} mismatches"
+    single = g.gemm(host(Af, "f32"), host(Bf, "f32", pad=2), alpha=2.0)
+    assert np.array_equal(result(single), result(outs[0]))
+
+
+def test_host_batch_of_one_and_empty():
+    seed = 14500
+    A = gi.draw("uniform", seed, 0, (700, 300))
+    B = gi.draw("uniform", seed, 1, (300, 500))
+    (one,) = g.gemm_many([dict(A=host(A, "f32"), B=host(B, "f32"))])
+    ref = g.gemm(host(A, "f32"), host(B, "f32"))
+    assert np.array_equal(one.numpy(), ref.numpy())  # same kernels, same order
+    assert g.gemm_many([]) == []
+
+
+def test_host_batch_rejects_a_result_feeding_another_product():
+    """Products of one batch run overlapped, so one product's result may not
+    be another's operand: the library refuses before copying anything."""
+    A = host(np.ones((64, 64), np.float32), "f32")
+    B = host(np.ones((64, 64), np.float32), "f32")
+    C1 = torch.zeros((64, 64), dtype=torch.float32).pin_memory()
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_many([dict(A=A, B=B, out=C1), dict(A=C1, B=B)])
+    assert e.value.status == g.binding.GEMM_ERR_ALIAS
+    assert float(C1.abs().max()) == 0.0  # untouched
