@@ -28,6 +28,7 @@ std::atomic<int64_t> g_cta_pair{0};
 std::atomic<int64_t> g_stream_k{0};
 std::atomic<int64_t> g_pair_limit{0};
 std::atomic<int64_t> g_stage_pairs{0};
+std::atomic<int64_t> g_kpair_maps_off{0};
 std::atomic<int64_t> g_last_fault{0};
 
 std::mutex g_state_mu;
@@ -141,7 +142,7 @@ RuntimeConfig runtime_config() {
     return RuntimeConfig{g_watchdog_ms.load(), g_force_path.load(), g_fault_inject.load(),
                          g_split_k.load(),      g_bf16_tile_n.load(), g_tail_split_off.load(),
                          g_raster_group.load(), g_cta_pair.load(), g_stream_k.load(),
-                         g_pair_limit.load(),   g_stage_pairs.load()};
+                         g_pair_limit.load(),   g_stage_pairs.load(), g_kpair_maps_off.load()};
 }
 
 void consume_fault_inject() { g_fault_inject.store(0); }
@@ -610,6 +611,9 @@ extern "C" int gemm_set_config(const char *key, int64_t value) {
     } else if (!strcmp(key, "stage_pairs")) {
         if (value < 0 || value > 2) return GEMM_ERR_INVALID_ARG;
         g_stage_pairs.store(value);
+    } else if (!strcmp(key, "kpair_maps_off")) {
+        if (value < 0 || value > 1) return GEMM_ERR_INVALID_ARG;
+        g_kpair_maps_off.store(value);
     } else {
         return GEMM_ERR_INVALID_ARG;
     }
@@ -629,6 +633,7 @@ extern "C" int gemm_get_config(const char *key, int64_t *value) {
     else if (!strcmp(key, "stream_k")) *value = g_stream_k.load();
     else if (!strcmp(key, "pair_limit")) *value = g_pair_limit.load();
     else if (!strcmp(key, "stage_pairs")) *value = g_stage_pairs.load();
+    else if (!strcmp(key, "kpair_maps_off")) *value = g_kpair_maps_off.load();
     else return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }

@@ -102,6 +102,8 @@ struct TcParams {
     // barrier wait and eight MMAs per pair of stages): 0 every unit, 1 the
     // narrower tail sub-tiles only, 2 none.
     int stage_pairs;
+    // CTA-pair kernel: the K-pair tensor maps are valid (see make_kpair_maps).
+    int kpair;
     float alpha, beta;
     void *C;
     long long ldc;
@@ -1006,7 +1008,8 @@ __device__ __forceinline__ bool stage_pairs_for(const TcParams &p, const Unit &w
 // CTA's full barrier.
 template <bool A_MN, bool B_KM, bool B3>
 __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMap *tmA,
-                                             const CUtensorMap *tmB, uint8_t *sA, uint8_t *sB,
+                                             const CUtensorMap *tmB, const CUtensorMap *tmA2,
+                                             const CUtensorMap *tmB2, uint8_t *sA, uint8_t *sB,
                                              uint64_t *full, uint64_t *empty,
                                              volatile int *abort_flag, uint32_t rank, int pair,
                                              int npairs) {
@@ -1046,6 +1049,35 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
                                       col0 + j * 64, k0, bb);
             }
         };
+        // K blocks kb and kb + 1 into stages st and st + 1 (back to back in
+        // shared memory) through the K-pair maps: one copy for this CTA's A
+        // rows, one for its B columns when they are 128 wide (else a
+        // 64-column box per stage, as load_stage).
+        auto load_two = [&](int st, int kb, uint32_t full_cl) {
+            uint8_t *a_dst = sA + st * Cfg::A_BYTES;
+            if constexpr (A_MN)
+                tma_load_4d_pair(a_dst, tmA2, full_cl, 0, 0, row0 / 64, kb);
+            else
+                tma_load_3d_pair(a_dst, tmA2, full_cl, 0, row0, kb);
+            uint8_t *b_dst = sB + st * Cfg::B_BYTES;
+            if (boxes == 2) {
+                if constexpr (B_KM)
+                    tma_load_3d_pair(b_dst, tmB2, full_cl, 0, col0, kb);
+                else
+                    tma_load_4d_pair(b_dst, tmB2, full_cl, 0, 0, col0 / 64, kb);
+                return;
+            }
+            for (int h = 0; h < 2; ++h) {
+                const int k0 = (kb + h) * TC_BK;
+                for (int j = 0; j < boxes; ++j) {
+                    uint8_t *d = b_dst + h * Cfg::B_BYTES + j * Cfg::B_BOX_BYTES;
+                    if constexpr (B_KM)
+                        load_box_pair<B3>(d, tmB, full_cl, k0, col0 + j * 64, bb);
+                    else
+                        load_box_pair<B3>(d, tmB, full_cl, col0 + j * 64, k0, bb);
+                }
+            }
+        };
         const bool paired = stage_pairs_for(p, w);
         for (int kb = w.kb0; kb < w.kb1 && ok;) {
             // Paired: K blocks kb and kb + 1 go to consecutive stages s and s2
@@ -1074,8 +1106,12 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
                 mbar_arrive_expect_tx(&full[s], (uint32_t)step * tx);
                 if (two) mbar_arrive(&full[s2]);
             }
-            load_stage(s, kb, full_cl);
-            if (two) load_stage(s2, kb + 1, full_cl);
+            if (!B3 && two && p.kpair && s2 == s + 1) {
+                load_two(s, kb, full_cl);
+            } else {
+                load_stage(s, kb, full_cl);
+                if (two) load_stage(s2, kb + 1, full_cl);
+            }
             it += step;
             kb += step;
         }
@@ -1093,29 +1129,33 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
 
 template <bool B3>
 __device__ __forceinline__ void tc2_produce_layout(const TcParams &p, const CUtensorMap *tmA,
-                                                   const CUtensorMap *tmB, uint8_t *sA,
+                                                   const CUtensorMap *tmB,
+                                                   const CUtensorMap *tmA2,
+                                                   const CUtensorMap *tmB2, uint8_t *sA,
                                                    uint8_t *sB, uint64_t *full, uint64_t *empty,
                                                    volatile int *abort_flag, uint32_t rank,
                                                    int pair, int npairs) {
     if (!p.a_mn && !p.b_kmaj)
-        tc2_producer<false, false, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag, rank, pair,
-                                       npairs);
+        tc2_producer<false, false, B3>(p, tmA, tmB, tmA2, tmB2, sA, sB, full, empty, abort_flag,
+                                       rank, pair, npairs);
     else if (!p.a_mn)
-        tc2_producer<false, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag, rank, pair,
-                                      npairs);
+        tc2_producer<false, true, B3>(p, tmA, tmB, tmA2, tmB2, sA, sB, full, empty, abort_flag,
+                                      rank, pair, npairs);
     else if (!p.b_kmaj)
-        tc2_producer<true, false, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag, rank, pair,
-                                      npairs);
+        tc2_producer<true, false, B3>(p, tmA, tmB, tmA2, tmB2, sA, sB, full, empty, abort_flag,
+                                      rank, pair, npairs);
     else
-        tc2_producer<true, true, B3>(p, tmA, tmB, sA, sB, full, empty, abort_flag, rank, pair,
-                                     npairs);
+        tc2_producer<true, true, B3>(p, tmA, tmB, tmA2, tmB2, sA, sB, full, empty, abort_flag,
+                                     rank, pair, npairs);
 }
 
 template <bool EPI, bool B3>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     bf16_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmC, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ CUtensorMap tmA2,
+                    const __grid_constant__ CUtensorMap tmB2, const TcParams p) {
     using Cfg = Tc2Cfg;
     constexpr int S = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
@@ -1157,6 +1197,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (p.kpair) {
+            prefetch_tensormap(&tmA2);
+            prefetch_tensormap(&tmB2);
+        }
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
@@ -1171,8 +1215,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            tc2_produce_layout<B3>(p, &tmA, &tmB, sA, sB, full, empty, abort_flag, rank, pair,
-                                   npairs);
+            tc2_produce_layout<B3>(p, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, abort_flag,
+                                   rank, pair, npairs);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -1595,9 +1639,9 @@ struct MapEntry {
     CUtensorMapDataType dtype;
     cuuint32_t rank;
     const void *base;
-    cuuint64_t dims[3];
-    cuuint64_t strides[2];
-    cuuint32_t box[3];
+    cuuint64_t dims[4];
+    cuuint64_t strides[3];
+    cuuint32_t box[4];
     CUtensorMapSwizzle swizzle;
     CUtensorMapL2promotion l2;
     CUtensorMap map;
@@ -1623,8 +1667,8 @@ bool encode_cached(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank,
         }
     }
     auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint32_t estr[3] = {1, 1, 1};
+    if (!fn || rank > 4) return false;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
     if (fn(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, l2, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
         CUDA_SUCCESS)
@@ -1637,11 +1681,11 @@ bool encode_cached(CUtensorMap *map, CUtensorMapDataType dtype, cuuint32_t rank,
     e.base = base;
     e.swizzle = swizzle;
     e.l2 = l2;
-    for (cuuint32_t i = 0; i < 3; ++i) {
+    for (cuuint32_t i = 0; i < 4; ++i) {
         e.dims[i] = i < rank ? dims[i] : 0;
         e.box[i] = i < rank ? box[i] : 0;
     }
-    for (cuuint32_t i = 0; i < 2; ++i) e.strides[i] = i + 1 < rank ? strides[i] : 0;
+    for (cuuint32_t i = 0; i < 3; ++i) e.strides[i] = i + 1 < rank ? strides[i] : 0;
     e.map = *map;
     return true;
 }
@@ -1703,6 +1747,65 @@ bool make_c_map(CUtensorMap *map, TcParams &p, int64_t batch) {
                          batch > 1 ? 3 : 2, p.C, dims, strides, box,
                          p.c_f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                          CU_TENSOR_MAP_L2_PROMOTION_NONE);
+}
+
+// K-pair tensor maps of the CTA-pair kernel: boxes that span two
+// consecutive 64-deep K blocks, so that one TMA copy fills an operand's part
+// of two ring stages (stages s and s + 1 lie back to back in shared memory,
+// and the box's outermost dimension walks the K blocks).  The K blocks
+// become a dimension of their own, 128 bytes apart: a K-major operand (K
+// contiguous) is viewed as 64 (k within the block) x rows x K/64 blocks, an
+// MN-major one as 64 (m or n within a 64-wide chunk) x 64 (k) x chunks x
+// K/64 blocks.  Such a view reads only inside the matrix when K is a
+// multiple of 64 and, for an MN-major operand, M or N is too (a K-major
+// view's rows past M or N are its own dimension's out-of-range rows, read as
+// zeros like the 2-D maps' ones).  One product only (no batch).  Sets
+// p.kpair when both maps are encoded; otherwise the kernel copies one K
+// block per box.  A whole tile's pair of stages then takes two copies per
+// CTA instead of six, which shortens the producer's turn between a stage
+// being freed and its refill (measured on GB300, N(0,1) data, L2 flushed:
+// 4096^3 85.5 -> 82.7 us, 8192 x 14336 x 4096 508.6 -> 489.8 us, 8192^3
+// 593.9 -> 579.7 us).
+void make_kpair_maps(CUtensorMap *ta, CUtensorMap *tb, TcParams &p, const uint16_t *A,
+                     int64_t lda, const uint16_t *B, int64_t ldb) {
+    p.kpair = 0;
+    memset(ta, 0, sizeof(*ta));
+    memset(tb, 0, sizeof(*tb));
+    const uint64_t M = (uint64_t)p.M, N = (uint64_t)p.N, K = (uint64_t)p.K;
+    if (K % 64 != 0 || (p.a_mn && M % 64 != 0) || (!p.b_kmaj && N % 64 != 0)) return;
+    const uint64_t kb = K / 64, pa = (uint64_t)lda * 2, pb = (uint64_t)ldb * 2;
+    const auto bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+    const auto l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+    bool ok;
+    if (p.a_mn) {  // A stored K x M: element (m, k) at k * lda + m
+        const cuuint64_t dims[4] = {64, 64, M / 64, kb};
+        const cuuint64_t str[3] = {pa, 128, 64 * pa};
+        const cuuint32_t box[4] = {64, TC_BK, TC_BM / 64, 2};
+        ok = encode_cached(ta, bf16, 4, A, dims, str, box, sw, l2);
+    } else {  // row-major A: element (m, k) at m * lda + k
+        const cuuint64_t dims[3] = {64, M, kb};
+        const cuuint64_t str[2] = {pa, 128};
+        const cuuint32_t box[3] = {TC_BK, TC_BM, 2};
+        ok = encode_cached(ta, bf16, 3, A, dims, str, box, sw, l2);
+    }
+    if (ok && p.b_kmaj) {  // B stored N x K: element (k, n) at n * ldb + k
+        const cuuint64_t dims[3] = {64, N, kb};
+        const cuuint64_t str[2] = {pb, 128};
+        const cuuint32_t box[3] = {TC_BK, 128, 2};
+        ok = encode_cached(tb, bf16, 3, B, dims, str, box, sw, l2);
+    } else if (ok) {  // row-major B: element (k, n) at k * ldb + n
+        const cuuint64_t dims[4] = {64, 64, N / 64, kb};
+        const cuuint64_t str[3] = {pb, 128, 64 * pb};
+        const cuuint32_t box[4] = {64, TC_BK, 2, 2};
+        ok = encode_cached(tb, bf16, 4, B, dims, str, box, sw, l2);
+    }
+    if (ok) {
+        p.kpair = 1;
+    } else {
+        memset(ta, 0, sizeof(*ta));
+        memset(tb, 0, sizeof(*tb));
+    }
 }
 
 template <int BN>
@@ -1912,9 +2015,16 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     int pairs_max = max_resident_pairs(device);
     if (pairs_max <= 0) return GEMM_ERR_CUDA;
     if (cfg.pair_limit > 0 && cfg.pair_limit < pairs_max) pairs_max = (int)cfg.pair_limit;
-    alignas(64) CUtensorMap ta, tb, tc;
+    alignas(64) CUtensorMap ta, tb, tc, ta2, tb2;
     if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb, o)) return GEMM_ERR_CUDA;
     if (!make_c_map(&tc, p, o.batch)) return GEMM_ERR_CUDA;
+    if (o.batch > 1 || cfg.kpair_maps_off || cfg.stage_pairs == 2) {
+        p.kpair = 0;
+        memset(&ta2, 0, sizeof(ta2));
+        memset(&tb2, 0, sizeof(tb2));
+    } else {
+        make_kpair_maps(&ta2, &tb2, p, A, lda, B, ldb);
+    }
     p.num_m_blk = (p.M + 2 * TC_BM - 1) / (2 * TC_BM);  // 256-row pair tiles
     p.num_n_blk = (p.N + Cfg::BN - 1) / Cfg::BN;
     p.num_kb = (p.K + TC_BK - 1) / TC_BK;
@@ -1972,11 +2082,13 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     lc.numAttrs = 1;
     cudaError_t e;
     if (o.batch > 1)
-        e = p.epi.on ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, true>, ta, tb, tc, p)
-                     : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, true>, ta, tb, tc, p);
+        e = p.epi.on
+                ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, true>, ta, tb, tc, ta2, tb2, p)
+                : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, true>, ta, tb, tc, ta2, tb2, p);
     else
-        e = p.epi.on ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, false>, ta, tb, tc, p)
-                     : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, false>, ta, tb, tc, p);
+        e = p.epi.on
+                ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, false>, ta, tb, tc, ta2, tb2, p)
+                : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, false>, ta, tb, tc, ta2, tb2, p);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

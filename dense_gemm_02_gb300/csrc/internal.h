@@ -104,6 +104,7 @@ struct RuntimeConfig {
     int64_t stream_k;
     int64_t pair_limit;
     int64_t stage_pairs;
+    int64_t kpair_maps_off;
 };
 RuntimeConfig runtime_config();
 void consume_fault_inject();

@@ -285,6 +285,15 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const void *map, uin
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d_pair(void *dst, const void *map, uint32_t mbar_cl,
+                                                 int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+        "bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cl), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(slot)),

@@ -396,6 +396,10 @@ GEMM_API const char *gemm_status_string(int status);
  *                   pair of stages; the single-CTA kernel only when its ring
  *                   has six or more stages), 1 on the CTA-pair kernel only its
  *                   narrower tail tiles, 2 none
+ *   "kpair_maps_off" 0 (default): where the shape allows, the CTA-pair
+ *                   kernel fills two stages with one TMA copy per operand
+ *                   (boxes spanning two 64-deep K blocks); 1: one copy per
+ *                   64-deep box
  * Returns GEMM_OK or GEMM_ERR_INVALID_ARG for an unknown key or value.
  */
 GEMM_API int gemm_set_config(const char *key, int64_t value);

@@ -163,7 +163,8 @@ def test_config_keys(lib):
     # every documented key round-trips its default and rejects a bad value
     for key, bad in (("force_path", 3), ("fault_inject", 2), ("split_k", 65), ("bf16_tile_n", 64),
                      ("tail_split_off", 2), ("stream_k", 2), ("raster_group", -1),
-                     ("cta_pair", 3), ("pair_limit", -1), ("stage_pairs", 3)):
+                     ("cta_pair", 3), ("pair_limit", -1), ("stage_pairs", 3),
+                     ("kpair_maps_off", 2)):
         v = b.get_config(key)
         b.set_config(key, v)
         with pytest.raises(b.GemmError):
