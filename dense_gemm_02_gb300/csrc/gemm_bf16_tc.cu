@@ -545,7 +545,11 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
                     ph ^= 1u;
                 }
             }
-            if (!mbar_wait(&empty[cur], cur_ph ^ 1u, abort_flag, p.timeout_ns) ||
+            // For two stages wait on the second one's empty barrier alone: the
+            // MMA thread commits stage nxt after stage cur, and a tcgen05
+            // commit arrives only once every earlier MMA of that thread has
+            // finished, so stage cur is free by then too.
+            if ((!two && !mbar_wait(&empty[cur], cur_ph ^ 1u, abort_flag, p.timeout_ns)) ||
                 (two && !mbar_wait(&empty[nxt], nxt_ph ^ 1u, abort_flag, p.timeout_ns))) {
                 record_fault(p, abort_flag, kRoleProducer, cur, w.tile);
                 ok = false;
@@ -1088,7 +1092,10 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
             const uint32_t ph = (it / S) & 1u;
             const int s2 = (it + 1) % S;
             const uint32_t ph2 = ((it + 1) / S) & 1u;
-            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns) ||
+            // For two stages wait on s2's empty barrier alone (its commit
+            // follows stage s's; see tc_producer).  Measured on GB300: 4096^3
+            // 82.9 -> 81.9 us.
+            if ((!two && !mbar_wait(&empty[s], ph ^ 1u, abort_flag, p.timeout_ns)) ||
                 (two && !mbar_wait(&empty[s2], ph2 ^ 1u, abort_flag, p.timeout_ns))) {
                 record_fault(p, abort_flag, kRoleProducer, s, w.tile);
                 ok = false;
