@@ -1013,7 +1013,8 @@ __device__ __forceinline__ bool stage_pairs_for(const TcParams &p, const Unit &w
 template <bool A_MN, bool B_KM, bool B3>
 __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMap *tmA,
                                              const CUtensorMap *tmB, const CUtensorMap *tmA2,
-                                             const CUtensorMap *tmB2, uint8_t *sA, uint8_t *sB,
+                                             const CUtensorMap *tmB2, const CUtensorMap *tmBh,
+                                             uint8_t *sA, uint8_t *sB,
                                              uint64_t *full, uint64_t *empty,
                                              volatile int *abort_flag, uint32_t rank, int pair,
                                              int npairs) {
@@ -1055,8 +1056,10 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
         };
         // K blocks kb and kb + 1 into stages st and st + 1 (back to back in
         // shared memory) through the K-pair maps: one copy for this CTA's A
-        // rows, one for its B columns when they are 128 wide (else a
-        // 64-column box per stage, as load_stage).
+        // rows and one for its B columns.  128 B columns fill both stages'
+        // B slots; 64 (a column-half tail tile) land in stage st's B slot
+        // alone, K block kb + 1 in its second 8 KiB, where the MMA warp
+        // reads them (b_half_packed).
         auto load_two = [&](int st, int kb, uint32_t full_cl) {
             uint8_t *a_dst = sA + st * Cfg::A_BYTES;
             if constexpr (A_MN)
@@ -1069,6 +1072,13 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
                     tma_load_3d_pair(b_dst, tmB2, full_cl, 0, col0, kb);
                 else
                     tma_load_4d_pair(b_dst, tmB2, full_cl, 0, 0, col0 / 64, kb);
+                return;
+            }
+            if (boxes == 1) {
+                if constexpr (B_KM)
+                    tma_load_3d_pair(b_dst, tmBh, full_cl, 0, col0, kb);
+                else
+                    tma_load_4d_pair(b_dst, tmBh, full_cl, 0, 0, col0 / 64, kb);
                 return;
             }
             for (int h = 0; h < 2; ++h) {
@@ -1138,22 +1148,23 @@ template <bool B3>
 __device__ __forceinline__ void tc2_produce_layout(const TcParams &p, const CUtensorMap *tmA,
                                                    const CUtensorMap *tmB,
                                                    const CUtensorMap *tmA2,
-                                                   const CUtensorMap *tmB2, uint8_t *sA,
+                                                   const CUtensorMap *tmB2,
+                                                   const CUtensorMap *tmBh, uint8_t *sA,
                                                    uint8_t *sB, uint64_t *full, uint64_t *empty,
                                                    volatile int *abort_flag, uint32_t rank,
                                                    int pair, int npairs) {
     if (!p.a_mn && !p.b_kmaj)
-        tc2_producer<false, false, B3>(p, tmA, tmB, tmA2, tmB2, sA, sB, full, empty, abort_flag,
-                                       rank, pair, npairs);
+        tc2_producer<false, false, B3>(p, tmA, tmB, tmA2, tmB2, tmBh, sA, sB, full, empty,
+                                       abort_flag, rank, pair, npairs);
     else if (!p.a_mn)
-        tc2_producer<false, true, B3>(p, tmA, tmB, tmA2, tmB2, sA, sB, full, empty, abort_flag,
-                                      rank, pair, npairs);
+        tc2_producer<false, true, B3>(p, tmA, tmB, tmA2, tmB2, tmBh, sA, sB, full, empty,
+                                      abort_flag, rank, pair, npairs);
     else if (!p.b_kmaj)
-        tc2_producer<true, false, B3>(p, tmA, tmB, tmA2, tmB2, sA, sB, full, empty, abort_flag,
-                                      rank, pair, npairs);
+        tc2_producer<true, false, B3>(p, tmA, tmB, tmA2, tmB2, tmBh, sA, sB, full, empty,
+                                      abort_flag, rank, pair, npairs);
     else
-        tc2_producer<true, true, B3>(p, tmA, tmB, tmA2, tmB2, sA, sB, full, empty, abort_flag,
-                                     rank, pair, npairs);
+        tc2_producer<true, true, B3>(p, tmA, tmB, tmA2, tmB2, tmBh, sA, sB, full, empty,
+                                     abort_flag, rank, pair, npairs);
 }
 
 template <bool EPI, bool B3>
@@ -1162,7 +1173,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ CUtensorMap tmA2,
-                    const __grid_constant__ CUtensorMap tmB2, const TcParams p) {
+                    const __grid_constant__ CUtensorMap tmB2,
+                    const __grid_constant__ CUtensorMap tmBh, const TcParams p) {
     using Cfg = Tc2Cfg;
     constexpr int S = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
@@ -1207,6 +1219,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (p.kpair) {
             prefetch_tensormap(&tmA2);
             prefetch_tensormap(&tmB2);
+            prefetch_tensormap(&tmBh);
         }
     }
     if (warp == 1) {
@@ -1222,8 +1235,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            tc2_produce_layout<B3>(p, &tmA, &tmB, &tmA2, &tmB2, sA, sB, full, empty, abort_flag,
-                                   rank, pair, npairs);
+            tc2_produce_layout<B3>(p, &tmA, &tmB, &tmA2, &tmB2, &tmBh, sA, sB, full, empty,
+                                   abort_flag, rank, pair, npairs);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -1256,9 +1269,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const uint32_t d_tmem = tmem_base + b * BN;
                 uint32_t acc = 0;
                 const bool paired = stage_pairs_for(p, w);
+                // Column-half tile whose paired K blocks were copied through
+                // the K-pair maps: the second block's B sits in the first
+                // stage's B slot, 8 KiB in (see tc2_producer).
+                const bool b_half_packed = !B3 && p.kpair && w.width == BN / 2;
                 for (int kb = w.kb0; kb < w.kb1;) {
                     // Paired: stages s and s + 1 both completed on full[s].
                     const bool two = paired && kb + 1 < w.kb1;
+                    const uint32_t s_first = s;
                     const bool ready = mbar_wait(&full[s], ph, abort_flag, p.timeout_ns);
                     if (__any_sync(0xffffffffu, !ready)) {
                         if (lane == 0) record_fault(p, abort_flag, kRoleMma, s, w.tile);
@@ -1280,7 +1298,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     if (two) {
                         const uint64_t ad2 = desc_add(a_desc0, s * Cfg::A_BYTES);
-                        const uint64_t bd2 = desc_add(b_desc0, s * Cfg::B_BYTES);
+                        const uint64_t bd2 =
+                            (b_half_packed && s_first + 1 < (uint32_t)S)
+                                ? desc_add(b_desc0, s_first * Cfg::B_BYTES + Cfg::B_BOX_BYTES)
+                                : desc_add(b_desc0, s * Cfg::B_BYTES);
                         umma_f16_pair_elect(d_tmem, ad2, bd2, idesc, 1u);
                         umma_f16_pair_elect(d_tmem, ad2 + a1, bd2 + b1, idesc, 1u);
                         umma_f16_pair_elect(d_tmem, ad2 + a2, bd2 + b2, idesc, 1u);
@@ -1653,7 +1674,7 @@ struct MapEntry {
     CUtensorMapL2promotion l2;
     CUtensorMap map;
 };
-constexpr int kMapCacheSize = 16;
+constexpr int kMapCacheSize = 32;
 thread_local MapEntry t_maps[kMapCacheSize];
 thread_local int t_next_map = 0;
 
@@ -1767,17 +1788,18 @@ bool make_c_map(CUtensorMap *map, TcParams &p, int64_t batch) {
 // multiple of 64 and, for an MN-major operand, M or N is too (a K-major
 // view's rows past M or N are its own dimension's out-of-range rows, read as
 // zeros like the 2-D maps' ones).  One product only (no batch).  Sets
-// p.kpair when both maps are encoded; otherwise the kernel copies one K
-// block per box.  A whole tile's pair of stages then takes two copies per
+// p.kpair when all three maps (A, B for whole tiles, B for column-half
+// tiles) are encoded; otherwise the kernel copies one K block per box.  A whole tile's pair of stages then takes two copies per
 // CTA instead of six, which shortens the producer's turn between a stage
 // being freed and its refill (measured on GB300, N(0,1) data, L2 flushed:
 // 4096^3 85.5 -> 82.7 us, 8192 x 14336 x 4096 508.6 -> 489.8 us, 8192^3
 // 593.9 -> 579.7 us).
-void make_kpair_maps(CUtensorMap *ta, CUtensorMap *tb, TcParams &p, const uint16_t *A,
-                     int64_t lda, const uint16_t *B, int64_t ldb) {
+void make_kpair_maps(CUtensorMap *ta, CUtensorMap *tb, CUtensorMap *tbh, TcParams &p,
+                     const uint16_t *A, int64_t lda, const uint16_t *B, int64_t ldb) {
     p.kpair = 0;
     memset(ta, 0, sizeof(*ta));
     memset(tb, 0, sizeof(*tb));
+    memset(tbh, 0, sizeof(*tbh));
     const uint64_t M = (uint64_t)p.M, N = (uint64_t)p.N, K = (uint64_t)p.K;
     if (K % 64 != 0 || (p.a_mn && M % 64 != 0) || (!p.b_kmaj && N % 64 != 0)) return;
     const uint64_t kb = K / 64, pa = (uint64_t)lda * 2, pb = (uint64_t)ldb * 2;
@@ -1796,22 +1818,29 @@ void make_kpair_maps(CUtensorMap *ta, CUtensorMap *tb, TcParams &p, const uint16
         const cuuint32_t box[3] = {TC_BK, TC_BM, 2};
         ok = encode_cached(ta, bf16, 3, A, dims, str, box, sw, l2);
     }
+    // tb: this CTA's 128 B columns of a whole tile; tbh: its 64 columns of
+    // a column-half tail tile.
     if (ok && p.b_kmaj) {  // B stored N x K: element (k, n) at n * ldb + k
         const cuuint64_t dims[3] = {64, N, kb};
         const cuuint64_t str[2] = {pb, 128};
         const cuuint32_t box[3] = {TC_BK, 128, 2};
-        ok = encode_cached(tb, bf16, 3, B, dims, str, box, sw, l2);
+        const cuuint32_t box_h[3] = {TC_BK, 64, 2};
+        ok = encode_cached(tb, bf16, 3, B, dims, str, box, sw, l2) &&
+             encode_cached(tbh, bf16, 3, B, dims, str, box_h, sw, l2);
     } else if (ok) {  // row-major B: element (k, n) at k * ldb + n
         const cuuint64_t dims[4] = {64, 64, N / 64, kb};
         const cuuint64_t str[3] = {pb, 128, 64 * pb};
         const cuuint32_t box[4] = {64, TC_BK, 2, 2};
-        ok = encode_cached(tb, bf16, 4, B, dims, str, box, sw, l2);
+        const cuuint32_t box_h[4] = {64, TC_BK, 1, 2};
+        ok = encode_cached(tb, bf16, 4, B, dims, str, box, sw, l2) &&
+             encode_cached(tbh, bf16, 4, B, dims, str, box_h, sw, l2);
     }
     if (ok) {
         p.kpair = 1;
     } else {
         memset(ta, 0, sizeof(*ta));
         memset(tb, 0, sizeof(*tb));
+        memset(tbh, 0, sizeof(*tbh));
     }
 }
 
@@ -2022,15 +2051,16 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     int pairs_max = max_resident_pairs(device);
     if (pairs_max <= 0) return GEMM_ERR_CUDA;
     if (cfg.pair_limit > 0 && cfg.pair_limit < pairs_max) pairs_max = (int)cfg.pair_limit;
-    alignas(64) CUtensorMap ta, tb, tc, ta2, tb2;
+    alignas(64) CUtensorMap ta, tb, tc, ta2, tb2, tbh;
     if (!make_ab_maps(&ta, &tb, p, A, lda, B, ldb, o)) return GEMM_ERR_CUDA;
     if (!make_c_map(&tc, p, o.batch)) return GEMM_ERR_CUDA;
     if (o.batch > 1 || cfg.kpair_maps_off || cfg.stage_pairs == 2) {
         p.kpair = 0;
         memset(&ta2, 0, sizeof(ta2));
         memset(&tb2, 0, sizeof(tb2));
+        memset(&tbh, 0, sizeof(tbh));
     } else {
-        make_kpair_maps(&ta2, &tb2, p, A, lda, B, ldb);
+        make_kpair_maps(&ta2, &tb2, &tbh, p, A, lda, B, ldb);
     }
     p.num_m_blk = (p.M + 2 * TC_BM - 1) / (2 * TC_BM);  // 256-row pair tiles
     p.num_n_blk = (p.N + Cfg::BN - 1) / Cfg::BN;
@@ -2090,12 +2120,12 @@ int launch_tc2(int device, TcParams &p, const uint16_t *A, int64_t lda, const ui
     cudaError_t e;
     if (o.batch > 1)
         e = p.epi.on
-                ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, true>, ta, tb, tc, ta2, tb2, p)
-                : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, true>, ta, tb, tc, ta2, tb2, p);
+                ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, true>, ta, tb, tc, ta2, tb2, tbh, p)
+                : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, true>, ta, tb, tc, ta2, tb2, tbh, p);
     else
         e = p.epi.on
-                ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, false>, ta, tb, tc, ta2, tb2, p)
-                : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, false>, ta, tb, tc, ta2, tb2, p);
+                ? cudaLaunchKernelEx(&lc, bf16_tc2_kernel<true, false>, ta, tb, tc, ta2, tb2, tbh, p)
+                : cudaLaunchKernelEx(&lc, bf16_tc2_kernel<false, false>, ta, tb, tc, ta2, tb2, tbh, p);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -1,8 +1,9 @@
 """GPU parity of the CTA-pair kernel's K-pair copies.  Where K is a multiple
 of 64 (and, for an operand stored MN-major, its M or N too), one TMA copy per
 operand fills two consecutive ring stages: the tensor map views the K blocks
-as a dimension of their own and its box spans two of them.  Column-half tail
-tiles copy A that way and B one 64-column box per stage.  A pair of stages
+as a dimension of their own and its box spans two of them.  A column-half
+tail tile's 64 B columns of both K blocks land in the first stage's B slot,
+where the MMA warp reads the second block.  A pair of stages
 that would wrap around the end of the ring (an odd K-block count shifts
 them) falls back to one copy per K block.  "kpair_maps_off" 1 turns the
 path off.

@@ -483,7 +483,7 @@ def test_tensor_map_reuse_across_calls_integer():
     or output type, and repeats)."""
     M, N, K = 384, 520, 264
     bufs = []
-    for i in range(10):
+    for i in range(14):
         A = gi.draw("integer", 19000 + i, 0, (M, K), dtype="bf16")
         B = gi.draw("integer", 19000 + i, 1, (K, N), dtype="bf16")
         bufs.append((A, B, bf16_to_dev(A), bf16_to_dev(B)))
