@@ -42,7 +42,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s (BF16 tcgen05, FP32 SIMT) at 4096^3 and % of chip peak"
-STEP_WORKLOADS = ("sgemm_4096", "bf16_4096")
+# The step's products, in launch order.  The BF16 product runs first, right
+# after the L2 flush like every other timed call: behind the SGEMM it reads
+# its operands while L2 writes back the SGEMM's 64 MiB of dirty C lines
+# (measured on GB300: 83.8 against 80.9 us; the SGEMM takes 2.127 ms either
+# way).
+STEP_WORKLOADS = ("bf16_4096", "sgemm_4096")
 FLUSH_BYTES = 256 << 20
 WARM_REPS = 20  # back-to-back calls per kernel in the warm-L2 context pass
 # L2-flushed calls timed for each workload outside the headline step
@@ -712,12 +717,16 @@ def run_ours(args, dist):
         outs = [torch.empty((w.M, w.N), dtype=od, pin_memory=True)
                 for (w, _a, _b, _c, od) in host_ops]
 
+        # The host batch overlaps a product's copies with the compute of the
+        # products before it, so the long FP32 product goes first.
+        e2e_ops = sorted(zip(host_ops, outs), key=lambda t: t[0][0].dtype != "f32")
+
         def e2e_step():
             # One call for the step's products: the copies of each travel while
             # the one before it computes (gemm_host_batch).
             g.gemm_many([dict(A=hA, B=hB, C=hC, alpha=w.alpha, beta=w.beta, out_dtype=od,
                               out=out)
-                         for (w, hA, hB, hC, od), out in zip(host_ops, outs)])
+                         for (w, hA, hB, hC, od), out in e2e_ops])
 
         for _ in range(2):
             e2e_step()

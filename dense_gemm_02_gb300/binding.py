@@ -24,6 +24,7 @@ GEMM_ERR_DEVICE_TIMEOUT = -6
 GEMM_ERR_ALIAS = -7
 GEMM_ERR_TOO_LARGE = -8
 GEMM_ERR_SCRATCH_LIMIT = -9
+GEMM_ERR_DEVICE_CHECK = -10
 
 GEMM_OUT_BF16 = 0
 GEMM_OUT_F32 = 1
@@ -90,6 +91,7 @@ SIGNATURES = {
     "gemm_noalloc_get_status": (_int, [_vp, ctypes.POINTER(_i64)]),
     "gemm_get_device_status": (_int, [_vp]),
     "gemm_get_device_fault_info": (_i64, []),
+    "gemm_debug_checks": (_int, []),
     "gemm_status_string": (_cp, [_int]),
     "gemm_set_config": (_int, [_cp, _i64]),
     "gemm_get_config": (_int, [_cp, ctypes.POINTER(_i64)]),
@@ -110,8 +112,14 @@ class GemmError(RuntimeError):
         super().__init__(f"{where}: {status_string(status)} ({status})")
 
 
+def debug_build_requested() -> bool:
+    """Whether this process loads the checked variant of the library
+    (environment variable GEMM_GB300_DEBUG=1)."""
+    return os.environ.get("GEMM_GB300_DEBUG", "0") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if debug_build_requested() else _build.LIB_PATH
 
 
 def lib():
@@ -120,10 +128,11 @@ def lib():
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
+        path = library_path()
         if not os.path.exists(path):
+            what = "the debug build " if debug_build_requested() else ""
             raise RuntimeError(
-                f"libgemm_gb300.so is not built ({path}); run "
+                f"{what}{os.path.basename(path)} is not built ({path}); run "
                 "`python -c 'import __graft_entry__ as g; g.build()'` first")
         handle = ctypes.CDLL(path)
         for name, (res, args) in SIGNATURES.items():
@@ -254,6 +263,11 @@ def get_device_status(stream=None) -> int:
 
 def get_device_fault_info() -> int:
     return int(lib().gemm_get_device_fault_info())
+
+
+def debug_checks() -> bool:
+    """Whether the loaded library is the debug build."""
+    return bool(lib().gemm_debug_checks())
 
 
 def set_config(key: str, value: int) -> None:

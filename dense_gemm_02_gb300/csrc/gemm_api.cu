@@ -552,10 +552,12 @@ extern "C" int gemm_get_device_status(void *stream) {
                 return GEMM_ERR_CUDA;
     }
     if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
-    return GEMM_ERR_DEVICE_TIMEOUT;
+    return fault_status(word);
 }
 
 extern "C" int64_t gemm_get_device_fault_info(void) { return g_last_fault.load(); }
+
+extern "C" int gemm_debug_checks(void) { return GEMM_DEBUG ? 1 : 0; }
 
 extern "C" const char *gemm_status_string(int status) {
     switch (status) {
@@ -572,6 +574,8 @@ extern "C" const char *gemm_status_string(int status) {
         case GEMM_ERR_TOO_LARGE: return "GEMM_ERR_TOO_LARGE: dimension exceeds 2^31-1";
         case GEMM_ERR_SCRATCH_LIMIT:
             return "GEMM_ERR_SCRATCH_LIMIT: needs more split-K scratch than the static maximum";
+        case GEMM_ERR_DEVICE_CHECK:
+            return "GEMM_ERR_DEVICE_CHECK: a debug-build device check failed (access skipped)";
         default: return "unknown gemm status";
     }
 }

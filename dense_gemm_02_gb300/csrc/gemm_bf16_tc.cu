@@ -112,6 +112,7 @@ struct TcParams {
     int c_tma;  // C is written by TMA stores through shared memory
     float *ws;
     unsigned *counters;
+    int ws_tiles;  // tiles the split-K workspace and counters cover (checked in the debug build)
     unsigned long long *fault_word;
     unsigned long long timeout_ns;
     int fault_inject;
@@ -442,7 +443,8 @@ __device__ __forceinline__ void store_chunk_tma(const TcParams &p, float alpha, 
         // A chunk wholly outside C stores nothing, but still closes a
         // (then empty) group so that the buffer-reuse wait above always
         // refers to the store issued two chunks earlier.
-        if (gm0 < p.M && gn < p.N) {
+        if (gm0 < p.M && gn < p.N &&
+            debug_check(p.fault_word, gn % (p.c_f32 ? 4 : 8) == 0, kSiteStoreC, 0)) {
             if constexpr (B3)
                 tma_store_3d(tmC, buf, gn, gm0, bidx);
             else
@@ -512,6 +514,15 @@ __device__ __forceinline__ void tc_producer(const TcParams &p, const CUtensorMap
             uint8_t *a_dst = ring + st * (uint32_t)p.stage_bytes;
             uint8_t *b_dst = a_dst + p.a_slot;
             const int k0 = kb * TC_BK;
+            // Debug build: innermost (x) coordinates a multiple of 8 bf16
+            // elements (16 bytes); the copies inside stage st of the ring.
+            if (!debug_check(p.fault_word, st < S && (A_MN ? m0 % 8 : k0 % 8) == 0 &&
+                                               (int)a_tx <= p.a_slot,
+                             kSiteLoadA, w.tile) ||
+                !debug_check(p.fault_word, (B_KM ? k0 % 8 : w.n0 % 8) == 0 &&
+                                               p.a_slot + boxes * Cfg::B_BOX_BYTES <= p.stage_bytes,
+                             kSiteLoadB, w.tile))
+                return;
             if constexpr (A_MN) {
                 load_box<B3>(a_dst, tmA, bar, m0, k0, ab);
                 if (p.a_rows > 64) load_box<B3>(a_dst + 8192, tmA, bar, m0 + 64, k0, ab);
@@ -763,6 +774,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
+                if (!debug_check(p.fault_word, b * BN + w.width <= Cfg::TMEM_COLS, kSiteTmem,
+                                 w.tile)) {
+                    ok = false;
+                    break;
+                }
                 uint32_t acc = 0;
                 const bool paired = single_cta_pairs(p);
                 for (int kb = w.kb0; kb < w.kb1;) {
@@ -864,7 +880,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 // ((q * BN/32 + chunk) * 8 + j) * 32 + lane holds columns
                 // chunk * 32 + 4j .. +3 of row q * 32 + lane); warps whose 32
                 // rows all lie past M skip it.
-                const bool rows_in = w.m_blk * TC_BM + q * 32 < p.M;
+                const bool rows_in = w.m_blk * TC_BM + q * 32 < p.M &&
+                                     debug_check(p.fault_word,
+                                                 tile < p.ws_tiles && w.part < p.max_parts,
+                                                 kSiteWorkspace, w.tile);
                 const size_t slice4 = (size_t)TC_BM * BN / 4;
                 float4 *wq = reinterpret_cast<float4 *>(p.ws) +
                              ((size_t)tile * p.max_parts + w.part) * slice4 +
@@ -1038,6 +1057,14 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
         auto load_stage = [&](int st, int kb, uint32_t full_cl) {
             uint8_t *a_dst = sA + st * Cfg::A_BYTES;
             const int k0 = kb * TC_BK;
+            // Debug build: x coordinates a multiple of 8 bf16 elements, the
+            // copies inside stage st's slots.
+            if (!debug_check(p.fault_word, st >= 0 && st < S && (A_MN ? row0 % 8 : k0 % 8) == 0,
+                             kSiteLoadA, w.tile) ||
+                !debug_check(p.fault_word, (B_KM ? k0 % 8 : col0 % 8) == 0 &&
+                                               boxes * Cfg::B_BOX_BYTES <= Cfg::B_BYTES,
+                             kSiteLoadB, w.tile))
+                return;
             if constexpr (A_MN) {
                 load_box_pair<B3>(a_dst, tmA, full_cl, row0, k0, ab);
                 load_box_pair<B3>(a_dst + 8192, tmA, full_cl, row0 + 64, k0, ab);
@@ -1061,6 +1088,14 @@ __device__ __forceinline__ void tc2_producer(const TcParams &p, const CUtensorMa
         // alone, K block kb + 1 in its second 8 KiB, where the MMA warp
         // reads them (b_half_packed).
         auto load_two = [&](int st, int kb, uint32_t full_cl) {
+            // Debug build: both stages inside the ring, the chunk coordinates
+            // of the K-pair views whole 64-element chunks.
+            if (!debug_check(p.fault_word, st >= 0 && st + 1 < S && (!A_MN || row0 % 64 == 0),
+                             kSiteLoadA, w.tile) ||
+                !debug_check(p.fault_word,
+                             B_KM || col0 % ((boxes == 1 || boxes == 2) ? 64 : 8) == 0,
+                             kSiteLoadB, w.tile))
+                return;
             uint8_t *a_dst = sA + st * Cfg::A_BYTES;
             if constexpr (A_MN)
                 tma_load_4d_pair(a_dst, tmA2, full_cl, 0, 0, row0 / 64, kb);
@@ -1267,6 +1302,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
+                if (!debug_check(p.fault_word, b * BN + w.width <= Cfg::TMEM_COLS, kSiteTmem,
+                                 w.tile)) {
+                    ok = false;
+                    break;
+                }
                 uint32_t acc = 0;
                 const bool paired = stage_pairs_for(p, w);
                 // Column-half tile whose paired K blocks were copied through
@@ -1298,10 +1338,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     }
                     if (two) {
                         const uint64_t ad2 = desc_add(a_desc0, s * Cfg::A_BYTES);
+                        const bool packed = b_half_packed && s_first + 1 < (uint32_t)S;
                         const uint64_t bd2 =
-                            (b_half_packed && s_first + 1 < (uint32_t)S)
-                                ? desc_add(b_desc0, s_first * Cfg::B_BYTES + Cfg::B_BOX_BYTES)
-                                : desc_add(b_desc0, s * Cfg::B_BYTES);
+                            packed ? desc_add(b_desc0, s_first * Cfg::B_BYTES + Cfg::B_BOX_BYTES)
+                                   : desc_add(b_desc0, s * Cfg::B_BYTES);
+                        if (!debug_check(p.fault_word,
+                                         s < (uint32_t)S && (!packed || s == s_first + 1),
+                                         kSiteSmemDesc, w.tile)) {
+                            ok = false;
+                            break;
+                        }
                         umma_f16_pair_elect(d_tmem, ad2, bd2, idesc, 1u);
                         umma_f16_pair_elect(d_tmem, ad2 + a1, bd2 + b1, idesc, 1u);
                         umma_f16_pair_elect(d_tmem, ad2 + a2, bd2 + b2, idesc, 1u);
@@ -1501,6 +1547,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     uint8_t *a_dst = ring + cur * (uint32_t)p.stage_bytes;
                     uint8_t *b_dst = a_dst + a_slot;
                     const int k0 = kb * TC_BK;
+                    // Debug build: x coordinates a multiple of 8 bf16 elements,
+                    // the group index inside the launch's table.
+                    if (!debug_check(p.fault_word, g >= 0 && g < p.groups && cur < S &&
+                                                       (A_MN ? m0 % 8 : k0 % 8) == 0,
+                                     kSiteLoadA, u) ||
+                        !debug_check(p.fault_word, (B_KM ? k0 % 8 : n0 % 8) == 0, kSiteLoadB,
+                                     u))
+                        continue;
                     if constexpr (A_MN) {
                         tma_load_2d(a_dst, &p.ma[g], &full[cur], m0, k0);
                         tma_load_2d(a_dst + 8192, &p.ma[g], &full[cur], m0 + 64, k0);
@@ -1551,6 +1605,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             tc_fence_after_sync();
             const uint32_t d_tmem = tmem_base + b * BN;
+            if (!debug_check(p.fault_word, b * BN + BN <= Cfg::TMEM_COLS, kSiteTmem, u)) {
+                ok = false;
+                break;
+            }
             uint32_t acc = 0;
             for (int kb = 0; kb < nkb; ++kb) {
                 const bool ready = mbar_wait(&full[s], ph, abort_flag, p.timeout_ns);
@@ -1957,7 +2015,9 @@ int launch_tc(int device, int sm_count, DeviceState *st, const ExternalScratch *
     p.num_units = (int)units;
     p.ws = nullptr;
     p.counters = nullptr;
+    p.ws_tiles = 0;
     if (p.splits > 1 || p.stream_k) {
+        p.ws_tiles = (int)tiles;
         const size_t ws_bytes = (size_t)tiles * p.max_parts * TC_BM * BN * sizeof(float);
         if (ext) {
             if (ws_bytes > ext->ws_bytes || (size_t)tiles > ext->counters_n)

@@ -129,5 +129,5 @@ extern "C" int gemm_noalloc_get_status(void *stream, int64_t *fault_info) {
     if (word == 0) return GEMM_OK;
     if (fault_info) *fault_info = (int64_t)(word & ~kFaultFlag);
     if (cudaMemset(rec, 0, sizeof(word)) != cudaSuccess) return GEMM_ERR_CUDA;
-    return GEMM_ERR_DEVICE_TIMEOUT;
+    return fault_status(word);
 }

@@ -42,7 +42,13 @@ class PerDeviceOnce {
 // Device fault word layout (written once per fault by the first failing
 // thread with atomicCAS; 0 means no fault).
 constexpr unsigned long long kFaultFlag = 1ull << 63;
-enum FaultRole : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleSimt = 4 };
+enum FaultRole : unsigned {
+    kRoleProducer = 1,
+    kRoleMma = 2,
+    kRoleEpilogue = 3,
+    kRoleSimt = 4,
+    kRoleCheck = 5  // a debug-build check failed; the stage byte holds its CheckSite
+};
 
 __host__ __device__ constexpr unsigned long long fault_code(unsigned role, unsigned stage,
                                                             unsigned tile) {
@@ -50,6 +56,47 @@ __host__ __device__ constexpr unsigned long long fault_code(unsigned role, unsig
            ((unsigned long long)(stage & 0xff) << 8) |
            ((unsigned long long)tile << 16);
 }
+
+// Status a nonzero fault word reports: GEMM_ERR_DEVICE_CHECK for a failed
+// debug-build check, else GEMM_ERR_DEVICE_TIMEOUT (a wait ran out).
+inline int fault_status(unsigned long long word) {
+    return (word & 0xff) == kRoleCheck ? GEMM_ERR_DEVICE_CHECK : GEMM_ERR_DEVICE_TIMEOUT;
+}
+
+// Debug build (compiled with GEMM_DEBUG=1 into libgemm_gb300_debug.so):
+// device-side checks of the indices, copy coordinates and shared- and
+// tensor-memory ranges the kernels compute.  A failed check records
+// kRoleCheck and its site in the fault word (the first fault wins) and its
+// caller skips the access it guards; waits that depended on that access then
+// run out and the kernel leaves through its usual watchdog path.  In the
+// release build every check is the constant true and compiles away.
+#ifndef GEMM_DEBUG
+#define GEMM_DEBUG 0
+#endif
+enum CheckSite : unsigned {
+    kSiteLoadA = 1,      // a TMA load of A: x coordinate alignment, destination range
+    kSiteLoadB = 2,      // the same for B
+    kSiteStoreC = 3,     // a TMA store of C: x coordinate alignment, staging range
+    kSiteTmem = 4,       // an accumulator's tensor-memory columns
+    kSiteWorkspace = 5,  // a split-K partial tile or counter index
+    kSiteSmemDesc = 6    // an MMA operand's shared-memory range
+};
+
+#if defined(__CUDACC__)
+__device__ __forceinline__ bool debug_check(unsigned long long *fault_word, bool ok,
+                                            unsigned site, unsigned tile) {
+#if GEMM_DEBUG
+    if (!ok) atomicCAS(fault_word, 0ull, fault_code(kRoleCheck, site, tile));
+    return ok;
+#else
+    (void)fault_word;
+    (void)ok;
+    (void)site;
+    (void)tile;
+    return true;
+#endif
+}
+#endif
 
 // Split-K workspace of one stream: fp32 partial tiles and one uint32
 // counter per split tile (each counter is back at zero after every launch).

@@ -69,6 +69,7 @@ struct TmaParams {
     long long c_bstride;
     float *ws;           // fp32 partial tiles of the split tiles
     unsigned *counters;  // one per split tile
+    int ws_tiles;        // split tiles the workspace covers (checked in the debug build)
 };
 
 // The work of one CTA: output tile (m_blk, n_blk) of matrix bidx of the
@@ -107,8 +108,11 @@ __device__ __forceinline__ void sgemm_cta(const CUtensorMap *tmA, const CUtensor
         const int s = kt % TSTAGES;
         uint8_t *st = smem + s * TSTAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], TSTAGE_BYTES);
-        tma_load_3d(st, tmA, &full[s], (kt0 + kt) * TBK, m0, ab);
-        tma_load_3d(st + TA_BYTES, tmB, &full[s], n0, (kt0 + kt) * TBK, bb);
+        // Debug build: x coordinates a multiple of 4 fp32 elements (16 bytes).
+        if (debug_check(p.fault_word, ((kt0 + kt) * TBK) % 4 == 0, kSiteLoadA, (unsigned)tile))
+            tma_load_3d(st, tmA, &full[s], (kt0 + kt) * TBK, m0, ab);
+        if (debug_check(p.fault_word, n0 % 4 == 0, kSiteLoadB, (unsigned)tile))
+            tma_load_3d(st + TA_BYTES, tmB, &full[s], n0, (kt0 + kt) * TBK, bb);
     };
     int issued = 0;
     if (tid == 0)
@@ -197,6 +201,9 @@ __device__ __forceinline__ void sgemm_cta(const CUtensorMap *tmA, const CUtensor
         // arrive add all slices in the fixed order 0..splits-1, so the result
         // does not depend on which slice finishes last.
         const size_t split_tile = (size_t)(tile - p.tiles_main);
+        if (!debug_check(p.fault_word, split_tile < (size_t)p.ws_tiles && slice < p.splits,
+                         kSiteWorkspace, (unsigned)tile))
+            return;
         float4 *base = reinterpret_cast<float4 *>(p.ws) + split_tile * p.splits * (16 * TTHREADS);
         float4 *mine = base + (size_t)slice * (16 * TTHREADS);
 #pragma unroll
@@ -443,6 +450,7 @@ int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const fl
     p.kt_per_split = 0;
     p.ws = nullptr;
     p.counters = nullptr;
+    p.ws_tiles = 0;
     const int KT = (K + TBK - 1) / TBK;
     const long long sms = st->sm_count;
     if (!runtime_config().tail_split_off && sms > 0) {
@@ -476,6 +484,7 @@ int launch_sgemm_tma(DeviceState *st, int M, int N, int K, float alpha, const fl
         if (rc != GEMM_OK) return rc;
         p.ws = w->ws;
         p.counters = w->counters;
+        p.ws_tiles = (int)split_tiles;
     }
     sgemm_tma_kernel<<<(unsigned)units, TTHREADS, TSMEM_ALLOC, stream>>>(ta, tb, p);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;

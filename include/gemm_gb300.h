@@ -81,8 +81,12 @@ typedef enum {
     GEMM_ERR_DEVICE_TIMEOUT = -6,     /* a pipeline wait on the GPU ran out of time */
     GEMM_ERR_ALIAS = -7,              /* C overlaps A, B or the bias */
     GEMM_ERR_TOO_LARGE = -8,          /* a dimension or pitch exceeds 2^31 - 1 */
-    GEMM_ERR_SCRATCH_LIMIT = -9       /* gemm_bf16_noalloc: the call needs more split-K
+    GEMM_ERR_SCRATCH_LIMIT = -9,      /* gemm_bf16_noalloc: the call needs more split-K
                                          scratch than its static maximum */
+    GEMM_ERR_DEVICE_CHECK = -10       /* debug build only (libgemm_gb300_debug.so): a
+                                         device-side check of an index, a copy's
+                                         coordinates or a shared/tensor-memory range
+                                         failed and the access was skipped */
 } gemm_status_t;
 
 typedef enum {
@@ -341,7 +345,8 @@ GEMM_API int gemm_bf16_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
  * counterpart).  Synchronises `stream` (make it the stream, or the last of
  * the streams, the calls ran on), reads the static array's fault record and
  * returns GEMM_OK if no wait ran out since the record was last read, else
- * GEMM_ERR_DEVICE_TIMEOUT and clears the record.  fault_info (may be NULL)
+ * GEMM_ERR_DEVICE_TIMEOUT (GEMM_ERR_DEVICE_CHECK for a failed check of the
+ * debug build) and clears the record.  fault_info (may be NULL)
  * receives the fault's details in the layout of
  * gemm_get_device_fault_info, or 0.  GEMM_ERR_CUDA if a CUDA call failed.
  * Like the first gemm_bf16_noalloc call, the first use on a device looks up
@@ -352,20 +357,37 @@ GEMM_API int gemm_noalloc_get_status(void *stream, int64_t *fault_info);
 /*
  * Synchronises `stream`, then returns and clears the current device's
  * pipeline status: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a kernel since the
- * last call gave up on a wait (its output is then incomplete).  Returns
- * GEMM_ERR_CUDA if the synchronisation itself failed.
+ * last call gave up on a wait (its output is then incomplete), or, in the
+ * debug build (libgemm_gb300_debug.so, loaded when the environment variable
+ * GEMM_GB300_DEBUG is 1), GEMM_ERR_DEVICE_CHECK if a device-side check of an
+ * index, a copy coordinate or a memory range failed (the checked access was
+ * skipped; the output is then incomplete).  Returns GEMM_ERR_CUDA if the
+ * synchronisation itself failed.
  */
 GEMM_API int gemm_get_device_status(void *stream);
 
 /*
  * Details of the last recorded device fault (0 if none): bits 0-7 the role
- * (1 producer, 2 MMA issuer, 3 epilogue, 4 FP32 kernel), bits 8-15 the pipeline stage,
- * bits 16-47 the tile index.  Does not clear it.
+ * (1 producer, 2 MMA issuer, 3 epilogue, 4 FP32 kernel, 5 a debug-build
+ * check), bits 8-15 the pipeline stage (for a check: its site, 1 a load of
+ * A, 2 a load of B, 3 a store of C, 4 tensor-memory columns, 5 a split-K
+ * workspace index, 6 an MMA operand's shared-memory range), bits 16-47 the
+ * tile index.  Does not clear it.
  */
 GEMM_API int64_t gemm_get_device_fault_info(void);
 
 /* A static, human-readable name for a gemm_status_t. */
 GEMM_API const char *gemm_status_string(int status);
+
+/*
+ * 1 in the debug build (libgemm_gb300_debug.so, compiled with GEMM_DEBUG=1,
+ * whose kernels check the indices, copy coordinates and shared/tensor-memory
+ * ranges they compute and report a failed check as GEMM_ERR_DEVICE_CHECK),
+ * 0 in the release build.  Needs no GPU.  Part of the library's own
+ * test support (compute-sanitizer is not available to its tests); the source
+ * pages have no counterpart.
+ */
+GEMM_API int gemm_debug_checks(void);
 
 /*
  * Tuning and debugging knobs (process-wide).  Keys:

@@ -58,6 +58,25 @@ def test_only_declared_symbols_are_exported(lib):
     assert ours == set(declared_functions())
 
 
+def test_release_and_debug_builds_report_their_variant(lib):
+    """The debug build (GEMM_DEBUG=1) builds from the same sources, exports
+    the same C ABI and says it is the debug build; the release build says it
+    is not.  Loading needs no GPU."""
+    from dense_gemm_02_gb300 import _build, binding
+
+    assert lib.gemm_debug_checks() == 0
+    assert not binding.debug_build_requested() or binding.library_path() == _build.DEBUG_LIB_PATH
+    path = _build.build(debug=True)
+    assert path == _build.DEBUG_LIB_PATH and path != _build.LIB_PATH
+    dbg = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"{name} declared but not exported by the debug build"
+    dbg.gemm_debug_checks.restype = ctypes.c_int
+    assert dbg.gemm_debug_checks() == 1
+    dbg.gemm_status_string.restype = ctypes.c_char_p
+    assert dbg.gemm_status_string(-10).decode().startswith("GEMM_ERR_DEVICE_CHECK")
+
+
 def test_status_strings_and_version(lib):
     from dense_gemm_02_gb300 import binding as b
 

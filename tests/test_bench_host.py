@@ -80,7 +80,7 @@ def test_parse_variant_rejects_unknown_items():
 
 def test_workload_selection():
     step = bench.workloads_for("step")
-    assert [w.name for w in step] == ["sgemm_4096", "bf16_4096"]
+    assert [w.name for w in step] == ["bf16_4096", "sgemm_4096"]
     assert bench.workloads_for("bf16_decode_64x8192x8192")[0].M == 64
     with pytest.raises(SystemExit):
         bench.workloads_for("no_such_workload")
