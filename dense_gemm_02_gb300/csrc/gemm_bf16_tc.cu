@@ -2310,8 +2310,9 @@ int launch_common(int device, int sm_count, DeviceState *st, const ExternalScrat
         bn = (N <= 128) ? 128 : 256;
         // When 256-wide tiles are too few for the SMs (the split-K regime),
         // 128-wide tiles need half as many K slices for the same parallelism:
-        // less partial-sum traffic and a shorter reduction (measured on the
-        // 64 x 8192 x 8192 shape: 42 us vs 52 us).
+        // less partial-sum traffic and a shorter reduction (measured on
+        // GB300, 64 x 8192 x 8192 -> fp32, L2 flushed: 35.0 us against 38.8
+        // us; 64 x 4096 x 14336: 33.2 against 43.1 us).
         const long long tiles256 =
             (long long)((M + TC_BM - 1) / TC_BM) * ((N + 255) / 256) * o.batch;
         if (bn == 256 && tiles256 * 2 <= sm_count && (K + TC_BK - 1) / TC_BK >= 8 &&
