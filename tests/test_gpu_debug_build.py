@@ -2,9 +2,9 @@
 GPU.  Its kernels check the copy coordinates (a TMA x coordinate must be a
 multiple of 16 bytes), the shared- and tensor-memory ranges and the split-K
 workspace indices they compute; a failed check skips the access, records
-its site and surfaces as GEMM_ERR_DEVICE_CHECK.  compute-sanitizer is not
-available here, so this build is how the tests look for out-of-range
-indices the guard bands around C cannot see.
+its site and surfaces as GEMM_ERR_DEVICE_CHECK.  Without compute-sanitizer,
+the debug library is how the tests look for out-of-range indices the guard
+bands around C cannot see.
 
 The parity tests of the kernels' edge paths run again in a child process
 that loads the debug build (GEMM_GB300_DEBUG=1): the CTA-pair kernel's K-pair
