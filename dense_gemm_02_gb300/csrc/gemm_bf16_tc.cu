@@ -1463,8 +1463,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t tempty_cl1 = mapa_shared(smem_addr(&tempty[1]), 0);
         uint64_t *cbar = cload + 2 * q;
         // beta != 0 with TMA stores: C is loaded through the staging buffers
-        // (store_chunk_tma_cload), and each warp asks L2 for its 32 rows of
-        // the unit's C while the unit's MMAs run.
+        // (store_chunk_tma_cload).  (Also asking L2 for each unit's C while
+        // its MMAs ran measured no different.)
         const bool cload_path = p.beta != 0.f && p.c_tma;
         uint32_t local = 0;
         for (int u = pair; u < p.num_units; u += npairs) {
@@ -1472,16 +1472,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (w.n0 >= p.N) continue;
             const uint32_t b = local & 1u, use = local >> 1;
             ++local;
-            if (cload_path && lane == 0) {
-                const int gm0 = w.m_blk * 2 * TC_BM + (int)rank * TC_BM + q * 32;
-                if (gm0 < p.M)
-                    for (int c = 0; c < w.width / 32 && w.n0 + c * 32 < p.N; ++c) {
-                        if constexpr (B3)
-                            tma_prefetch_l2_3d(&tmC, w.n0 + c * 32, gm0, w.bidx);
-                        else
-                            tma_prefetch_l2_2d(&tmC, w.n0 + c * 32, gm0);
-                    }
-            }
             if (et == 0) {
                 const bool ok = mbar_wait(&tfull[b], use & 1u, abort_flag, p.timeout_ns);
                 if (!ok) record_fault(p, abort_flag, kRoleEpilogue, 0xff, w.tile);

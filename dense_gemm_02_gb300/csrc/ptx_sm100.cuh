@@ -152,22 +152,6 @@ __device__ __forceinline__ void tma_store_3d(const void *map, const void *src, i
         : "memory");
 }
 
-// Hint: bring a tensor map's box at the given coordinates into L2 (no
-// completion to wait for; boxes past the tensor's edge read nothing).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const void *map, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void *map, int c0, int c1, int c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
