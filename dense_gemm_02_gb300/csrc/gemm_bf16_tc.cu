@@ -492,7 +492,10 @@ __device__ __forceinline__ void store_chunk_tma_cload(const TcParams &p, float a
         }
     }
     __syncwarp();
-    if (!mbar_wait(bar, parity, abort_flag, p.timeout_ns) && lane == 0)
+    // Waits even when another role has raised the abort flag (bounded by
+    // the time limit), so that no load into buf is still in flight when the
+    // buffer is rewritten or the CTA exits.
+    if (!mbar_wait(bar, parity, abort_flag, p.timeout_ns, true) && lane == 0)
         record_fault(p, abort_flag, kRoleEpilogue, 0xfc, 0);
     if (p.c_f32) {
 #pragma unroll
