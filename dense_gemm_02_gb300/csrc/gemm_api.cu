@@ -667,4 +667,4 @@ extern "C" int gemm_shutdown(void) {
     return GEMM_OK;
 }
 
-extern "C" int gemm_abi_version(void) { return 1; }
+extern "C" int gemm_abi_version(void) { return 2; }

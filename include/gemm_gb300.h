@@ -439,7 +439,12 @@ GEMM_API const char *gemm_last_kernel(void);
 /* Frees the per-device state of the current device.  Safe to call twice. */
 GEMM_API int gemm_shutdown(void);
 
-/* Library ABI version, currently 1. */
+/*
+ * Library ABI version, currently 2.  Version 2 keeps every version-1 entry
+ * point and structure unchanged and adds gemm_bf16_grouped /
+ * gemm_f32_grouped, gemm_host_batch (gemm_host_op_t), gemm_noalloc_get_status,
+ * gemm_debug_checks and the status GEMM_ERR_DEVICE_CHECK.
+ */
 GEMM_API int gemm_abi_version(void);
 
 #ifdef __cplusplus

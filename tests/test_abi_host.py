@@ -80,7 +80,7 @@ def test_release_and_debug_builds_report_their_variant(lib):
 def test_status_strings_and_version(lib):
     from dense_gemm_02_gb300 import binding as b
 
-    assert b.abi_version() == 1
+    assert b.abi_version() == 2
     for code in range(-8, 1):
         assert b.status_string(code).startswith("GEMM_")
     assert "unknown" in b.status_string(42)
